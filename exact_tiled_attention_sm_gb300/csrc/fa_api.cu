@@ -1,0 +1,237 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument checks, TMA
+// descriptors, kernel selection and launch.  No device memory is allocated
+// here; every tensor and the backward workspace belong to the caller.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+#include "fa_common.cuh"
+#include "fa_internal.h"
+#include "fa_sched.cuh"
+
+#define FA_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int checked = 0;  // 0 unknown, 1 ok
+  int sm_major = 0, sm_minor = 0, num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                   void*, const cuuint64_t*, const cuuint64_t*,
+                                   const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fa_status current_device(int* dev, DeviceInfo* info) {
+  if (cudaGetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[*dev];
+  if (!d.checked) {
+    if (cudaDeviceGetAttribute(&d.sm_major, cudaDevAttrComputeCapabilityMajor,
+                               *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_minor, cudaDevAttrComputeCapabilityMinor,
+                               *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount,
+                               *dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    d.checked = 1;
+  }
+  *info = d;
+  return FA_OK;
+}
+
+fa_status get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return FA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                       cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return FA_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return FA_OK;
+}
+
+// [B*H, N, d] bf16 tensor; boxes of 64 columns x 128 rows x 1 head, 128-byte
+// swizzle, out-of-range rows read as zero.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) {
+  return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+fa_status check_shape(int B, int H, int N, int d, float scale, int dt) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (dt != FA_BF16 && dt != FA_F32) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long elems = (long long)B * H * N * d;
+  if (elems >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H >= (1ll << 31) / 128) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+fa_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
+                        float* LSE, int B, int H, int N, int d, float scale,
+                        int causal, fa_dtype dt, void* stream) {
+  fa_status st = check_shape(B, H, N, d, scale, (int)dt);
+  if (st != FA_OK) return st;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      !aligned16(LSE))
+    return FA_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo info;
+  if ((st = current_device(&dev, &info)) != FA_OK) return st;
+  const fa::AttnShape s{B, H, N, d, scale, causal ? 1 : 0};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == FA_F32)
+    return from_cuda(fa::launch_fwd_f32(
+        s, static_cast<const float*>(Q), static_cast<const float*>(K),
+        static_cast<const float*>(V), static_cast<float*>(O), LSE, cs));
+  if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
+  if ((st = get_encoder()) != FA_OK) return st;
+  fa::TileMaps maps;
+  const int BH = B * H;
+  if ((st = make_map(&maps.q, Q, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
+  return from_cuda(fa::launch_fwd_tc(s, maps, O, LSE, info.num_sms,
+                                     fa::kWaitLimitNs, cs));
+}
+
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
+
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
+                        const void* O, const void* dO, const float* LSE,
+                        void* dQ, void* dK, void* dV, int B, int H, int N,
+                        int d, float scale, int causal, fa_dtype dt,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_shape(B, H, N, d, scale, (int)dt);
+  if (st != FA_OK) return st;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      !aligned16(dO) || !aligned16(LSE) || !aligned16(dQ) || !aligned16(dK) ||
+      !aligned16(dV))
+    return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < fa_bwd_workspace_size(B, H, N, d))
+    return FA_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo info;
+  if ((st = current_device(&dev, &info)) != FA_OK) return st;
+  const fa::AttnShape s{B, H, N, d, scale, causal ? 1 : 0};
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)B * H * N;
+  float* Dvec = static_cast<float*>(workspace);
+  float* dQacc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align256(rows * sizeof(float)));
+  if (dt == FA_F32) {
+    if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 0, Dvec, nullptr, cs))) !=
+        FA_OK)
+      return st;
+    return from_cuda(fa::launch_bwd_f32(
+        s, static_cast<const float*>(Q), static_cast<const float*>(K),
+        static_cast<const float*>(V), static_cast<const float*>(dO), LSE, Dvec,
+        static_cast<float*>(dQ), static_cast<float*>(dK),
+        static_cast<float*>(dV), cs));
+  }
+  if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
+  if ((st = get_encoder()) != FA_OK) return st;
+  fa::TileMaps maps;
+  const int BH = B * H;
+  if ((st = make_map(&maps.q, Q, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.dO, dO, BH, N, d)) != FA_OK) return st;
+  if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, dQacc, cs))) !=
+      FA_OK)
+    return st;
+  if ((st = from_cuda(fa::launch_bwd_tc(s, maps, LSE, Dvec, dQacc, dK, dV,
+                                        info.num_sms, fa::kWaitLimitNs, cs))) !=
+      FA_OK)
+    return st;
+  return from_cuda(fa::launch_dq_convert(s, dQacc, dQ, cs));
+}
+
+FA_API fa_status fa_last_device_status(void* stream) {
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned int words[3] = {fa::read_status_fwd_tc(cs),
+                                 fa::read_status_bwd_tc(cs),
+                                 fa::read_status_simt(cs)};
+  fa_status out = FA_OK;
+  for (unsigned int w : words) {
+    if (w == 0xFFFFFFFFu) return FA_ERR_CUDA;
+    if (w != 0 && out == FA_OK) out = static_cast<fa_status>(w & 0xFFu);
+  }
+  return out;
+}
+
+FA_API const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+FA_API fa_status fa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 10000000u) return FA_ERR_INVALID_ARG;
+  return from_cuda(fa::launch_selftest_timeout((uint64_t)limit_us * 1000ull,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+FA_API fa_status fa_fwd_schedule_census(int N, int causal, long long* out) {
+  if (N < 1 || !out) return FA_ERR_INVALID_ARG;
+  fa::FwdSched sc;
+  sc.init(1, N, causal ? 1 : 0, 1);
+  long long computed = 0;
+  for (int q = 0; q < sc.n_q_tiles; ++q) computed += sc.n_kv(q);
+  out[0] = computed;
+  out[1] = (long long)sc.n_q_tiles * sc.n_kv_total - computed;
+  out[2] = sc.n_pairs;
+  return FA_OK;
+}
+
+FA_API int fa_version(void) { return 100; }

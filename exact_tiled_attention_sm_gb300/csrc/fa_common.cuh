@@ -1,0 +1,40 @@
+// fa_common.cuh -- definitions shared by every kernel translation unit.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+
+namespace fa {
+
+// Device status word of this translation unit: 0, or FA_ERR_TIMEOUT in the
+// low byte with the id of the wait site that gave up in bits 8..15.  Each
+// kernel .cu file has its own copy (no relocatable device code), read and
+// cleared through that file's status reader.
+static __device__ unsigned int g_fa_device_status = 0;
+
+// Default limit of every bounded wait inside a kernel: far above any wait a
+// correct launch makes on the sizes this library accepts.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+constexpr int kTile = 128;  // rows of a query block and of a key block
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace fa
+
+// Defines `unsigned int NAME(cudaStream_t)` that synchronises the stream,
+// returns this file's status word and clears it.  Returns 0xFFFFFFFF if the
+// CUDA calls fail.
+#define FA_DEFINE_STATUS_READER(NAME)                                          \
+  unsigned int NAME(cudaStream_t stream) {                                     \
+    unsigned int v = 0, zero = 0;                                              \
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return 0xFFFFFFFFu;      \
+    if (cudaMemcpyFromSymbol(&v, fa::g_fa_device_status, sizeof(v)) !=        \
+        cudaSuccess)                                                           \
+      return 0xFFFFFFFFu;                                                      \
+    if (v != 0 && cudaMemcpyToSymbol(fa::g_fa_device_status, &zero,            \
+                                     sizeof(zero)) != cudaSuccess)             \
+      return 0xFFFFFFFFu;                                                      \
+    return v;                                                                  \
+  }

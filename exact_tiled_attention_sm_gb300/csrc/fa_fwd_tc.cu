@@ -1,0 +1,495 @@
+// fa_fwd_tc.cu -- bf16 exact attention forward on sm_103a tensor cores.
+//
+// One persistent CTA per SM walks the work items of FwdSched (one head, two
+// 128-row query blocks).  Roles, by warp:
+//   warps 0-3  softmax group 0: owns query block 0 of the item (TMEM lanes
+//              0-127, one thread per query row)
+//   warps 4-7  softmax group 1: query block 1
+//   warp  8    tensor-core issuer (one elected thread) and TMEM owner
+//   warp  9    TMA producer (one elected thread)
+//
+// Data flow per key/value block j ("LLM Architecture Refresh [3]", section 4:
+// queries outer, key/value blocks inner; "FlashAttention from scratch",
+// Steps 1-3):
+//   TMA    K_j, V_j  HBM -> shared memory (128-byte swizzled, 2-4 stage ring)
+//   MMA    S_t = Q_t K_j^T             (tcgen05, fp32 accumulator in TMEM)
+//   softmax t: S_t -> registers, scale by scale*log2(e), mask the diagonal /
+//          ragged block, m_new = max(m, rowmax), alpha = 2^(m - m_new),
+//          P = 2^(S - m_new) (bf16, written back over S_t in TMEM),
+//          l = alpha*l + rowsum(P), O_t *= alpha when the max moved
+//   MMA    O_t += P_t V_j              (A operand straight from TMEM)
+// and after the last block O = O_t / l, LSE = (m + log2 l) * ln 2 (the
+// division deferred to the end, "FlashAttention from scratch", Step 3).
+// The two query blocks ping-pong: while softmax group 0 works on S_0 the
+// tensor core runs group 1's S_1 and P_1 V products, and vice versa.
+//
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+d), O_1 [256+d, 256+2d); P_t aliases the first 64 columns of
+// S_t as packed bf16 pairs.
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "fa_sched.cuh"
+#include "fa_tiles.cuh"
+
+namespace fa {
+namespace fwdtc {
+
+template <int D>
+struct Cfg {
+  static constexpr int CH = D / 64;               // 128-byte column chunks
+  static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = CH * CHUNK_BYTES;
+  static constexpr int KST = (D == 64) ? 4 : 2;   // K ring stages
+  static constexpr int VST = (D == 64) ? 4 : 2;   // V ring stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
+  // barrier slots
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1;
+  static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + KST;
+  static constexpr int B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST;
+  static constexpr int B_SFULL = B_VEMPTY + VST;  // [2]
+  static constexpr int B_PREADY = B_SFULL + 2;    // [2]
+  static constexpr int B_ODONE = B_PREADY + 2;    // [2]
+  static constexpr int B_MMADONE = B_ODONE + 2;
+  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 4;
+  static constexpr uint32_t TM_S = 0;     // + 128 * t
+  static constexpr uint32_t TM_O = 256;   // + D * t
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
+};
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+
+struct Params {
+  __nv_bfloat16* O;
+  float* LSE;
+  float scale_log2;  // scale * log2(e)
+  uint64_t wait_limit_ns;
+  FwdSched sched;
+};
+
+// Wait-site ids recorded with a timeout.
+enum : uint32_t {
+  SITE_P_QEMPTY = 1, SITE_P_KEMPTY, SITE_P_VEMPTY, SITE_M_QFULL, SITE_M_KFULL,
+  SITE_M_VFULL, SITE_M_PREADY, SITE_S_SFULL, SITE_S_ODONE, SITE_DRAIN,
+  SITE_ALIGN
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap mq,
+               const __grid_constant__ CUtensorMap mk,
+               const __grid_constant__ CUtensorMap mv, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar0 = sb + C::OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+  volatile uint32_t* tmem_slot =
+      reinterpret_cast<volatile uint32_t*>(smem + C::OFF_TMEM);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const FwdSched& sc = p.sched;
+  const uint64_t lim = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QFULL), 1);
+    mbar_init(bar(C::B_QEMPTY), 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(bar(C::B_VFULL + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_SFULL + t), 1);
+      mbar_init(bar(C::B_PREADY + t), 128);
+      mbar_init(bar(C::B_ODONE + t), 1);
+    }
+    mbar_init(bar(C::B_MMADONE), 1);
+    // the swizzled tiles need 1024-byte alignment: refuse to run otherwise
+    *abort_flag = (sb & 1023u) ? 1 : 0;
+    if (sb & 1023u) record_timeout(abort_flag, SITE_ALIGN);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto sQ = [&](int t) { return sb + C::OFF_Q + (uint32_t)t * C::TILE_BYTES; };
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&mq);
+      prefetch_tensormap(&mk);
+      prefetch_tensormap(&mv);
+      uint32_t kcnt = 0, vcnt = 0, it = 0;
+      int last_q = -1;
+      // per ring stage: bit s of *_used = a copy was issued into stage s,
+      // bit s of *_par = the phase parity of the last such copy
+      uint32_t k_used = 0, k_par = 0, v_used = 0, v_par = 0;
+      const int nw = sc.n_waves();
+      for (int w = 0; w < nw && !*abort_flag; ++w) {
+        const int item = sc.item_of(blockIdx.x, w);
+        if (item < 0) continue;
+        int bh, pair;
+        sc.decode(item, bh, pair);
+        const int q0 = 2 * pair;
+        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        const int n_kv = sc.n_kv(valid1 ? q0 + 1 : q0);
+        if (it > 0 &&
+            !wait_one(bar(C::B_QEMPTY), (it - 1) & 1, abort_flag, lim,
+                      SITE_P_QEMPTY))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_QFULL),
+                              (valid1 ? 2 : 1) * C::TILE_BYTES);
+        for (int t = 0; t < (valid1 ? 2 : 1); ++t)
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(sQ(t) + c * C::CHUNK_BYTES, &mq, bar(C::B_QFULL),
+                        c * 64, (q0 + t) * 128, bh);
+        last_q = it & 1;
+        bool ok = true;
+        for (int j = 0; j < n_kv && ok; ++j) {
+          {
+            const int s = kcnt % C::KST;
+            const uint32_t ph = (kcnt / C::KST) & 1;
+            if (!wait_one(bar(C::B_KEMPTY + s), ph ^ 1, abort_flag, lim,
+                          SITE_P_KEMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
+            const uint32_t dst = sb + C::OFF_K + s * C::TILE_BYTES;
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(dst + c * C::CHUNK_BYTES, &mk, bar(C::B_KFULL + s),
+                          c * 64, j * 128, bh);
+            k_used |= 1u << s;
+            k_par = (k_par & ~(1u << s)) | (ph << s);
+            ++kcnt;
+          }
+          {
+            const int s = vcnt % C::VST;
+            const uint32_t ph = (vcnt / C::VST) & 1;
+            if (!wait_one(bar(C::B_VEMPTY + s), ph ^ 1, abort_flag, lim,
+                          SITE_P_VEMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
+            const uint32_t dst = sb + C::OFF_V + s * C::TILE_BYTES;
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(dst + c * C::CHUNK_BYTES, &mv, bar(C::B_VFULL + s),
+                          c * 64, j * 128, bh);
+            v_used |= 1u << s;
+            v_par = (v_par & ~(1u << s)) | (ph << s);
+            ++vcnt;
+          }
+        }
+        if (!ok) break;
+        ++it;
+      }
+      // Drain: every copy this thread issued must have landed before the CTA
+      // exits (normally all were consumed long ago and these return at once).
+      volatile int no_abort = 0;
+      if (last_q >= 0)
+        wait_one(bar(C::B_QFULL), (uint32_t)last_q, &no_abort, lim, SITE_DRAIN);
+      for (int s = 0; s < C::KST; ++s)
+        if ((k_used >> s) & 1)
+          wait_one(bar(C::B_KFULL + s), (k_par >> s) & 1, &no_abort, lim,
+                   SITE_DRAIN);
+      for (int s = 0; s < C::VST; ++s)
+        if ((v_used >> s) & 1)
+          wait_one(bar(C::B_VFULL + s), (v_par >> s) & 1, &no_abort, lim,
+                   SITE_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tensor core
+    if (lane == 0) {
+      uint32_t kcnt = 0, vcnt = 0, it = 0;
+      uint32_t pcnt0 = 0, pcnt1 = 0;
+      const int nw = sc.n_waves();
+      for (int w = 0; w < nw && !*abort_flag; ++w) {
+        const int item = sc.item_of(blockIdx.x, w);
+        if (item < 0) continue;
+        int bh, pair;
+        sc.decode(item, bh, pair);
+        const int q0 = 2 * pair;
+        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        const int n_t0 = sc.n_kv(q0);
+        const int n_t1 = valid1 ? sc.n_kv(q0 + 1) : 0;
+        const int n_kv = n_t1 > n_t0 ? n_t1 : n_t0;
+        bool ok = wait_one(bar(C::B_QFULL), it & 1, abort_flag, lim, SITE_M_QFULL);
+        if (!ok) break;
+        tc_fence_after();
+        {  // S_t for key block 0
+          const int s = kcnt % C::KST;
+          if (!wait_one(bar(C::B_KFULL + s), (kcnt / C::KST) & 1, abort_flag,
+                        lim, SITE_M_KFULL))
+            break;
+          tc_fence_after();
+          const uint32_t sk = sb + C::OFF_K + s * C::TILE_BYTES;
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if ((t ? n_t1 : n_t0) > 0) {
+              mma_rows_x_rows<D>(tmem + C::TM_S + 128 * t, sQ(t), sk, C::IDESC_S);
+              umma_commit(bar(C::B_SFULL + t));
+            }
+          umma_commit(bar(C::B_KEMPTY + s));
+          ++kcnt;
+        }
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int vs = vcnt % C::VST;
+          if (!wait_one(bar(C::B_VFULL + vs), (vcnt / C::VST) & 1, abort_flag,
+                        lim, SITE_M_VFULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sv = sb + C::OFF_V + vs * C::TILE_BYTES;
+          const int ks = kcnt % C::KST;
+          const uint32_t sk = sb + C::OFF_K + ks * C::TILE_BYTES;
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nt = t ? n_t1 : n_t0;
+            if (!ok || j >= nt) continue;
+            uint32_t& pc = t ? pcnt1 : pcnt0;
+            if (!wait_one(bar(C::B_PREADY + t), pc & 1, abort_flag, lim,
+                          SITE_M_PREADY)) {
+              ok = false;
+              continue;
+            }
+            ++pc;
+            tc_fence_after();
+            mma_tmem_x_rows(tmem + C::TM_O + D * t, tmem + C::TM_S + 128 * t,
+                            sv, C::IDESC_PV, j > 0);
+            if (j == nt - 1) umma_commit(bar(C::B_ODONE + t));
+            if (j + 1 < nt) {
+              if (!k_ready) {
+                if (!wait_one(bar(C::B_KFULL + ks), (kcnt / C::KST) & 1,
+                              abort_flag, lim, SITE_M_KFULL)) {
+                  ok = false;
+                  continue;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+              mma_rows_x_rows<D>(tmem + C::TM_S + 128 * t, sQ(t), sk, C::IDESC_S);
+              umma_commit(bar(C::B_SFULL + t));
+            }
+          }
+          umma_commit(bar(C::B_VEMPTY + vs));
+          ++vcnt;
+          if (k_ready) {
+            umma_commit(bar(C::B_KEMPTY + ks));
+            ++kcnt;
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(C::B_QEMPTY));
+        ++it;
+      }
+      // every MMA issued by this thread completes before TMEM is released
+      umma_commit(bar(C::B_MMADONE));
+      volatile int no_abort = 0;
+      wait_one(bar(C::B_MMADONE), 0, &no_abort, lim, SITE_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;          // query block of the item
+    const int wq = warp & 3;          // TMEM lane quarter
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S + 128 * t;
+    const uint32_t tO = tmem + lane_off + C::TM_O + D * t;
+    const float sl2 = p.scale_log2;
+    uint32_t scnt = 0, ocnt = 0;
+    const int nw = sc.n_waves();
+    for (int w = 0; w < nw && !*abort_flag; ++w) {
+      const int item = sc.item_of(blockIdx.x, w);
+      if (item < 0) continue;
+      int bh, pair;
+      sc.decode(item, bh, pair);
+      const int q = 2 * pair + t;
+      if (q >= sc.n_q_tiles) continue;
+      const int nt = sc.n_kv(q);
+      const int row = q * 128 + wq * 32 + lane;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nt; ++j) {
+        if (!wait_warp(bar(C::B_SFULL + t), scnt & 1, abort_flag, lim,
+                       SITE_S_SFULL)) {
+          ok = false;
+          break;
+        }
+        ++scnt;
+        tc_fence_after();
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait();
+        reg_fence32(r0);
+        reg_fence32(r1);
+        reg_fence32(r2);
+        reg_fence32(r3);
+        float x[128];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(r0[i]) * sl2;
+          x[32 + i] = __uint_as_float(r1[i]) * sl2;
+          x[64 + i] = __uint_as_float(r2[i]) * sl2;
+          x[96 + i] = __uint_as_float(r3[i]) * sl2;
+        }
+        if (sc.needs_mask(q, j)) {
+          const int k0 = j * 128;
+          const int lim_k = sc.causal ? min(row + 1, sc.N) : sc.N;  // keys < lim_k visible
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (k0 + i >= lim_k) x[i] = -INFINITY;
+        }
+        float tmax = x[0];
+#pragma unroll
+        for (int i = 1; i < 128; ++i) tmax = fmaxf(tmax, x[i]);
+        const float m_new = fmaxf(m, tmax);
+        // a row with nothing visible yet keeps 0 as its reference
+        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2_approx(m - m_ref);  // m = -inf -> 0
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          x[i] = ex2_approx(x[i] - m_ref);
+          rs += x[i];
+        }
+        l = l * alpha + rs;
+        m = m_new;
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+          tmem_st32(tS + 0, pk);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            pk[i] = pack_bf16x2(x[64 + 2 * i], x[64 + 2 * i + 1]);
+          tmem_st32(tS + 32, pk);
+        }
+        // O_t *= alpha when this warp's rows moved their max (the previous
+        // P V product into O_t completed before S_t of this block did)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PREADY + t));
+      }
+      if (!ok) break;
+      if (!wait_warp(bar(C::B_ODONE + t), ocnt & 1, abort_flag, lim,
+                     SITE_S_ODONE))
+        break;
+      ++ocnt;
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool store = row < sc.N;
+      __nv_bfloat16* orow = p.O + ((size_t)bh * sc.N + (size_t)(store ? row : 0)) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+        uint4 v[4];
+        uint32_t* vw = reinterpret_cast<uint32_t*>(v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          vw[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                              __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = v[i];
+        }
+      }
+      if (store)
+        p.LSE[(size_t)bh * sc.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+      // all TMEM reads of O_t are done before the next item's first P V
+      // product (ordered by this group's next p_ready arrival)
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
+                   float* LSE, int num_sms, uint64_t lim, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static bool attr_done = false;  // per process; same value on every device
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(
+        fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  Params p;
+  p.O = reinterpret_cast<__nv_bfloat16*>(O);
+  p.LSE = LSE;
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.wait_limit_ns = lim;
+  const int BH = s.B * s.H;
+  FwdSched probe;
+  probe.init(BH, s.N, s.causal, num_sms);
+  const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
+  p.sched.init(BH, s.N, s.causal, grid);
+  fwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps.q, maps.k,
+                                                             maps.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fwdtc
+
+cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
+                          float* LSE, int num_sms, uint64_t wait_limit_ns,
+                          cudaStream_t stream) {
+  if (s.d == 64)
+    return fwdtc::launch<64>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+  return fwdtc::launch<128>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+}
+
+FA_DEFINE_STATUS_READER(read_status_fwd_tc)
+
+}  // namespace fa

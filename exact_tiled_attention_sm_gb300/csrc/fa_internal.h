@@ -1,0 +1,54 @@
+// fa_internal.h -- launchers shared between the C-ABI layer (fa_api.cu) and
+// the kernel translation units.  Host-only declarations.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+struct AttnShape {
+  int B, H, N, d;
+  float scale;
+  int causal;
+};
+
+// TMA descriptors of the bf16 [B*H, N, d] tensors, 64-column x 128-row boxes
+// with the 128-byte swizzle (built by fa_api.cu).
+struct TileMaps {
+  CUtensorMap q, k, v, o, dO;
+};
+
+// fa_fwd_tc.cu -- bf16 forward on tcgen05/TMEM.
+cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
+                          float* LSE, int num_sms, uint64_t wait_limit_ns,
+                          cudaStream_t stream);
+unsigned int read_status_fwd_tc(cudaStream_t stream);
+
+// fa_bwd_tc.cu -- bf16 backward on tcgen05/TMEM.
+cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
+                          const float* LSE, const float* Dvec, float* dQacc,
+                          void* dK, void* dV, int num_sms,
+                          uint64_t wait_limit_ns, cudaStream_t stream);
+unsigned int read_status_bwd_tc(cudaStream_t stream);
+
+// fa_simt.cu -- fp32 forward/backward on the CUDA cores, and the backward's
+// pre/post passes for both dtypes.
+cudaError_t launch_fwd_f32(const AttnShape& s, const float* Q, const float* K,
+                           const float* V, float* O, float* LSE,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
+                           const float* V, const float* dO, const float* LSE,
+                           const float* Dvec, float* dQ, float* dK, float* dV,
+                           cudaStream_t stream);
+// D = rowsum(dO * O) (fp32), and dQacc zeroed when non-null.
+cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
+                           int is_bf16, float* Dvec, float* dQacc,
+                           cudaStream_t stream);
+// dQ (bf16) = dQacc.
+cudaError_t launch_dq_convert(const AttnShape& s, const float* dQacc, void* dQ,
+                              cudaStream_t stream);
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream);
+unsigned int read_status_simt(cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,137 @@
+// fa_sched.cuh -- the forward kernel's causal tile scheduler (host + device).
+//
+// A work item is one head (b, h) and one pair of consecutive 128-row query
+// blocks (rows [256*pair, 256*pair + 256)).  For query block q, the key
+// blocks visited are j = 0 .. n_kv(q)-1 with n_kv(q) = q + 1 under the
+// causal mask and ceil(N/128) otherwise: a key block whose first key lies
+// after the query block's last row is never loaded or multiplied ("LLM
+// Architecture Refresh [3]", section 7), and only the diagonal block (and a
+// ragged last block) is masked element by element.
+//
+// Balance.  Causal items cost in proportion to (pair + 1), so items are
+// listed heaviest first, and a persistent grid takes them in waves of `grid`
+// items with the CTA order reversed on every other wave ("snake"), pairing a
+// heavy item with a light one.  Locality.  The list is grouped by heads:
+// `group` heads at a time, about one wave's worth, so the K/V blocks that a
+// wave's CTAs stream are shared through L2 instead of re-read from HBM.
+#pragma once
+
+namespace fa {
+
+struct FwdSched {
+  int BH, N, causal, grid;
+  int n_q_tiles, n_pairs, n_kv_total, group, total_items;
+
+  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size) {
+    BH = bh;
+    N = n;
+    causal = is_causal;
+    grid = grid_size;
+    n_q_tiles = (N + 127) / 128;
+    n_kv_total = n_q_tiles;
+    n_pairs = (n_q_tiles + 1) / 2;
+    int g = grid / n_pairs;
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    group = g;
+    total_items = BH * n_pairs;
+  }
+
+  // Number of waves a CTA walks through.
+  __host__ __device__ int n_waves() const {
+    return (total_items + grid - 1) / grid;
+  }
+
+  // Item taken by CTA `cta` in wave `w`, or -1 if that slot is past the end.
+  __host__ __device__ int item_of(int cta, int w) const {
+    int pos = (w & 1) ? (grid - 1 - cta) : cta;
+    int i = w * grid + pos;
+    return i < total_items ? i : -1;
+  }
+
+  // Item index -> (flat head bh, query-block pair).
+  __host__ __device__ void decode(int i, int& bh, int& pair) const {
+    const int per_group = group * n_pairs;
+    const int full_groups = BH / group;
+    const int full_items = full_groups * per_group;
+    int g, r, gs;
+    if (i < full_items) {
+      g = i / per_group;
+      r = i - g * per_group;
+      gs = group;
+    } else {
+      g = full_groups;
+      r = i - full_items;
+      gs = BH - full_groups * group;
+    }
+    pair = n_pairs - 1 - r / gs;  // heaviest pairs first within a group
+    bh = g * group + r % gs;
+  }
+
+  // Key blocks visited by query block q (q < n_q_tiles).
+  __host__ __device__ int n_kv(int q) const {
+    if (!causal) return n_kv_total;
+    return q + 1 < n_kv_total ? q + 1 : n_kv_total;
+  }
+
+  // Does key block j of query block q need an element mask?
+  __host__ __device__ bool needs_mask(int q, int j) const {
+    return (causal && j == q) || (j == n_kv_total - 1 && (N & 127) != 0);
+  }
+};
+
+// The backward kernel's scheduler: a work item is one head and one 128-key
+// block kb; the CTA keeps K_kb and V_kb resident and walks the query blocks
+// i = q_begin(kb) .. n_blk-1 (i >= kb under the causal mask: query blocks that
+// lie entirely before the key block see none of it).  Causal cost is
+// proportional to n_blk - kb, so items are listed kb-ascending (heaviest
+// first) inside head groups, and taken in snake waves as in FwdSched.
+struct BwdSched {
+  int BH, N, causal, grid;
+  int n_blk, group, total_items;
+
+  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size) {
+    BH = bh;
+    N = n;
+    causal = is_causal;
+    grid = grid_size;
+    n_blk = (N + 127) / 128;
+    int g = grid / n_blk;
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    group = g;
+    total_items = BH * n_blk;
+  }
+
+  __host__ __device__ int n_waves() const {
+    return (total_items + grid - 1) / grid;
+  }
+
+  __host__ __device__ int item_of(int cta, int w) const {
+    int pos = (w & 1) ? (grid - 1 - cta) : cta;
+    int i = w * grid + pos;
+    return i < total_items ? i : -1;
+  }
+
+  __host__ __device__ void decode(int i, int& bh, int& kb) const {
+    const int per_group = group * n_blk;
+    const int full_groups = BH / group;
+    const int full_items = full_groups * per_group;
+    int g, r, gs;
+    if (i < full_items) {
+      g = i / per_group;
+      r = i - g * per_group;
+      gs = group;
+    } else {
+      g = full_groups;
+      r = i - full_items;
+      gs = BH - full_groups * group;
+    }
+    kb = r / gs;
+    bh = g * group + r % gs;
+  }
+
+  __host__ __device__ int q_begin(int kb) const { return causal ? kb : 0; }
+};
+
+}  // namespace fa

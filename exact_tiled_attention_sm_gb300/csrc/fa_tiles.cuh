@@ -1,0 +1,64 @@
+// fa_tiles.cuh -- 128-row bf16 tiles in shared memory and the tcgen05 MMA
+// sequences over them.
+//
+// Shared-memory tile layout (what TMA writes with the 128-byte swizzle and a
+// 64-column x 128-row box): a [128 rows][D] bf16 tile is D/64 column chunks
+// of 16 KiB; in a chunk, row r occupies bytes [128r, 128r + 128) with its
+// 16-byte pieces XOR-permuted by (r mod 8).  Every chunk starts on a
+// 1024-byte boundary.
+//
+// Read as an MMA operand, such a tile is
+//   K-major  when the reduction runs along its columns (Q or K in S = QK^T),
+//   MN-major when the reduction runs along its rows    (V in O += PV).
+#pragma once
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kChunkBytes = 128 * 128;  // one 64-column chunk of 128 rows
+
+// D(128 x 128) (+)= A B^T with A, B both [128][Dk] K-major tiles (Dk/16 MMAs
+// of K = 16; the 16-element step moves 32 bytes inside a 128-byte row).
+template <int Dk>
+__device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t sa,
+                                                uint32_t sb, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < Dk / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+    umma_ss(d_tmem, sdesc_sw128(sa + off, 16, 1024),
+            sdesc_sw128(sb + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D(128 x Dn) (+)= A B with A (128 x 128) in TMEM (bf16 pairs, lanes = rows)
+// and B a [128][Dn] tile read MN-major (8 MMAs of K = 16 rows; a step moves
+// 16 rows = 2048 bytes; the Dn/64 chunks are kChunkBytes apart).
+__device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint32_t sb, uint32_t idesc,
+                                                bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_ts(d_tmem, a_tmem + kk * 8,
+            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// D(128 x Dn) = A B with A^T a [128 (K)][128 (M)] tile read MN-major (its
+// two 64-column chunks are the M runs) and B a [128 (K)][Dn] tile read
+// MN-major.
+__device__ __forceinline__ void mma_colsT_x_rows(uint32_t d_tmem, uint32_t sat,
+                                                 uint32_t sb, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_ss(d_tmem, sdesc_sw128(sat + kk * 16 * 128, kChunkBytes, 1024),
+            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
+            kk > 0 ? 1u : 0u);
+}
+
+// Byte offset of the 16-byte piece `p` (0..15 across a 128-element row) of
+// row r in the layout above.
+__device__ __forceinline__ uint32_t swz_offset(int r, int p) {
+  return (uint32_t)((p >> 3) * kChunkBytes + r * 128 + (((p & 7) ^ (r & 7)) << 4));
+}
+
+}  // namespace fa

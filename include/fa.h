@@ -1,0 +1,117 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention library (libfa.so) for one
+ * sm_103a GPU.
+ *
+ * What it computes.  For every batch b and head h, with Q, K, V the N x d
+ * slices of that head:
+ *
+ *     O = softmax(scale * Q K^T) V,        LSE_r = m_r + ln(l_r),
+ *
+ * tile by tile with an online softmax: a running row max m and a running row
+ * sum l rescale the partial output whenever a later key/value block raises
+ * the max, and the division by l happens once at the end ("Flash Attention,
+ * From First Principles", sections "Online softmax -- the game" through "The
+ * scaffold"; "LLM Architecture Refresh [3]", section 4).  The N x N score
+ * matrix never reaches device memory.  With causal != 0, key k is visible to
+ * query r only when k <= r (queries and keys share one length N); key blocks
+ * that lie entirely in the future are skipped and only diagonal blocks are
+ * masked ("LLM Architecture Refresh [3]", section 7).  The backward pass
+ * recomputes the probabilities from Q, K and the saved LSE,
+ * P = exp(scale*QK^T - LSE), and forms dV = P^T dO, dP = dO V^T,
+ * D = rowsum(dO * O), dS = P * (dP - D), dQ = scale * dS K,
+ * dK = scale * dS^T Q ("FlashAttention from scratch", follow-up "How do you
+ * implement the backward pass of flash attention?").
+ *
+ * Conventions shared by every entry point.
+ *   - Tensors are caller-owned device memory, contiguous, in [B][H][N][d]
+ *     order (batch, heads, sequence, head dimension), base pointers 16-byte
+ *     aligned.  O, dQ, dK, dV have the input dtype; LSE is fp32 [B][H][N],
+ *     natural log.
+ *   - dt = FA_BF16: bf16 inputs, fp32 accumulation on the tensor cores.
+ *     dt = FA_F32: fp32 inputs and arithmetic throughout (CUDA cores).
+ *   - d must be 64 or 128; N >= 1; B, H >= 1; B*H*N*d must fit in 2^31
+ *     elements per tensor; scale must be finite.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  The returned status covers argument checks and the
+ *     launch only; device-side failures (a bounded wait that ran out) are
+ *     reported by fa_last_device_status().
+ *   - Argument errors return before anything is launched.  The library
+ *     allocates no device memory in fa_fwd / fa_bwd.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned, bad scale  */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, unknown dtype, no sm_103a  */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed              */
+  FA_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out             */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/* Forward pass.  Reads Q, K, V; writes O and LSE.  Steps: schedule (causal
+ * tile skip), TMA tile loads, S = scale*Q K^T, diagonal/ragged masking,
+ * online softmax with deferred division, O += P V, epilogue.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA. */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
+                 float* LSE, int B, int H, int N, int d, float scale,
+                 int causal, fa_dtype dt, void* stream);
+
+/* Bytes of device workspace fa_bwd needs: an fp32 dQ accumulator
+ * [B][H][N][d] and D = rowsum(dO * O) [B][H][N], each 256-byte aligned.
+ * Returns 0 for sizes fa_bwd would reject. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass.  Reads Q, K, V, O, dO and the forward's LSE; writes dQ, dK,
+ * dV.  `workspace` is caller-owned device memory of at least
+ * fa_bwd_workspace_size() bytes (256-byte aligned); its contents on entry do
+ * not matter and on return are unspecified.  Steps: D and zeroed dQ
+ * accumulator; per key block, recompute S and P from LSE, dV += P^T dO,
+ * dP = dO V^T, dS = P*(dP - D), dK += scale*dS^T Q, dQacc += scale*dS K
+ * (fp32 atomics); dQ = dQacc converted to the input dtype.
+ * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for a short workspace. */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
+                 const void* dO, const float* LSE, void* dQ, void* dK,
+                 void* dV, int B, int H, int N, int d, float scale,
+                 int causal, fa_dtype dt, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status of
+ * this library's kernels on the current device: FA_OK, or FA_ERR_TIMEOUT if
+ * a bounded wait ran out since the last call (the kernel that gave up
+ * skipped its remaining work, so its outputs are incomplete).  FA_ERR_CUDA
+ * if the synchronisation itself failed. */
+fa_status fa_last_device_status(void* stream);
+
+/* Short English name of a status code (static storage). */
+const char* fa_status_string(fa_status s);
+
+/* Failure-detection self test: launches one CTA whose single wait is on a
+ * barrier that nothing ever completes, with the given time limit in
+ * microseconds (1..10,000,000).  The wait gives up, records FA_ERR_TIMEOUT
+ * and the kernel exits normally; fa_last_device_status() then reports it.
+ * Touches no user memory. */
+fa_status fa_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
+/* Host-side view of the forward scheduler for one head: how many 128x128
+ * (query block, key block) tiles the forward kernel computes and skips, and
+ * how many work items (pairs of 128-row query blocks) it schedules.  Pure
+ * host arithmetic, no GPU needed.  out = {computed, skipped, items}. */
+fa_status fa_fwd_schedule_census(int N, int causal, long long* out);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

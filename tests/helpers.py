@@ -1,0 +1,54 @@
+"""Shared test helpers: seeded inputs on the GPU, guard-banded outputs, and
+error measures.  The tolerances are the ones the library is held to:
+fp32 inputs max |err| <= 1e-5; bf16 inputs (fp32 accumulation) max |err| <=
+1e-2 on O and <= 1e-3 on LSE; gradients relative L2 error <= 1e-2."""
+import numpy as np
+import torch
+
+from exact_tiled_attention_sm_gb300 import inputs
+
+TOL_F32 = 1e-5
+TOL_O_BF16 = 1e-2
+TOL_LSE_BF16 = 1e-3
+TOL_GRAD_REL = 1e-2
+
+GUARD = 4096  # elements of canary on each side of an output
+
+
+def guarded(shape, dtype, fill=float("nan")):
+    """Returns (view, backing): ``view`` is a contiguous tensor of ``shape``
+    in the middle of ``backing``, prefilled with ``fill``, with GUARD canary
+    elements (value 1536.0, exact in bf16 and fp32) before and after it."""
+    n = int(np.prod(shape))
+    backing = torch.full((n + 2 * GUARD,), 1536.0, dtype=dtype, device="cuda")
+    view = backing[GUARD:GUARD + n].view(shape)
+    view.fill_(fill)
+    return view, backing
+
+
+def guards_intact(backing):
+    head = backing[:GUARD].float()
+    tail = backing[-GUARD:].float()
+    return bool(torch.all(head == 1536.0)) and bool(torch.all(tail == 1536.0))
+
+
+def to_dev(x):
+    return {k: v.to("cuda") for k, v in x.items()}
+
+
+def max_abs(a, b):
+    return float(np.max(np.abs(np.asarray(a, dtype=np.float64) - b))) if np.size(b) else 0.0
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a))
+
+
+def np64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def seeded(B, H, N, d, seed, dtype="bf16", with_dO=False):
+    return inputs.seeded_inputs(B, H, N, d, seed, dtype, with_dO)

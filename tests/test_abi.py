@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/fa.h declares, rejects bad arguments before launching anything, and
+its host-side scheduler census agrees with the pages' causal tile count."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_sm_gb300 as fa
+import oracle
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_tiled_attention_sm_gb300 import _build
+    _build.build()
+    return fa.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    decl = declared_symbols()
+    assert len(decl) >= 8
+    assert sorted(fa.EXPORTS) == decl
+    for name in decl:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert fa.fa_status_string(fa.FA_OK) == "ok"
+    assert fa.fa_status_string(fa.FA_ERR_TIMEOUT) == "device wait timed out"
+    assert fa.fa_version() >= 100
+
+
+def _fwd(**kw):
+    a = dict(Q=16, K=16, V=16, O=16, LSE=16, B=1, H=1, N=16, d=64, scale=0.1,
+             causal=0, dt=fa.FA_BF16, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"],
+                     a["N"], a["d"], a["scale"], a["causal"], a["dt"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(LSE=None), fa.FA_ERR_INVALID_ARG),
+    (dict(K=24), fa.FA_ERR_INVALID_ARG),          # not 16-byte aligned
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(dt=7), fa.FA_ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(B=1 << 20, H=1 << 10, N=1 << 10), fa.FA_ERR_INVALID_ARG),  # overflow
+])
+def test_fwd_rejects_bad_arguments(L, kw, expect):
+    assert _fwd(**kw) == expect
+
+
+def test_bwd_rejects_bad_arguments(L):
+    n = fa.fa_bwd_workspace_size(1, 1, 16, 64)
+    assert n >= 16 * 4 + 16 * 64 * 4
+    args = [256] * 9 + [1, 1, 16, 64, 0.1, 0, fa.FA_BF16]
+    # short workspace, null workspace, misaligned workspace
+    assert fa.fa_bwd(*args, 256, n - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(*args, None, n, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(*args, 272, n, None) == fa.FA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[6] = None  # dQ
+    assert fa.fa_bwd(*bad, 256, n, None) == fa.FA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[12] = 32   # d
+    assert fa.fa_bwd(*bad, 256, n, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_workspace_size(1, 1, 16, 48) == 0
+    assert fa.fa_bwd_workspace_size(0, 1, 16, 64) == 0
+
+
+def test_workspace_size_is_linear_in_N(L):
+    """The backward's scratch is O(N) per head and the forward's is zero:
+    nothing grows like N^2 ("LLM Architecture Refresh [3]", section 6)."""
+    sizes = [fa.fa_bwd_workspace_size(1, 32, n, 128) for n in (8192, 16384, 32768)]
+    assert sizes[1] == 2 * sizes[0] and sizes[2] == 2 * sizes[1]
+    assert sizes[2] == 32 * 32768 * (128 + 1) * 4
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 100, 128, 129, 1000, 2048, 4096, 8192, 16384, 32768])
+def test_schedule_census_matches_tile_walk(L, N, causal):
+    comp, skip, items = fa.fa_fwd_schedule_census(N, causal)
+    _, oc, os_ = oracle.tile_census(1, N, 128, 128, 128, causal)
+    assert (comp, skip) == (oc, os_)
+    nq = -(-N // 128)
+    assert items == -(-nq // 2)
+
+
+@pytest.mark.parametrize("N", [8192, 16384, 32768])
+def test_schedule_skips_closed_form_fraction(L, N):
+    """(B-1)/(2B) of the 128x128 tiles are skipped for B blocks a side
+    ("LLM Architecture Refresh [3]", section 7)."""
+    comp, skip, _ = fa.fa_fwd_schedule_census(N, True)
+    Bk = N // 128
+    assert comp + skip == Bk * Bk
+    assert skip * 2 * Bk == (Bk - 1) * Bk * Bk
+
+
+def test_library_has_no_oracle_symbols(L):
+    """The product library and the oracle share nothing."""
+    assert not hasattr(L, "oracle_fwd")
+    path = fa.LIB_PATH
+    data = open(path, "rb").read()
+    assert b"oracle_" not in data

@@ -1,0 +1,148 @@
+"""Forward parity of the CUDA path (through the C ABI) against the fp64 oracle
+on the same seeded inputs: small ragged shapes element by element, the named
+workloads at full size on sampled rows, and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_sm_gb300 as fa
+import oracle
+from exact_tiled_attention_sm_gb300 import inputs
+from tests import helpers as h
+from tests.conftest import load_golden
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd(x, scale, causal):
+    """Calls fa_fwd with NaN-prefilled, guard-banded O and LSE."""
+    q, k, v = (x[n].to("cuda") for n in ("Q", "K", "V"))
+    B, H, N, d = q.shape
+    o, ob = h.guarded((B, H, N, d), q.dtype)
+    lse, lb = h.guarded((B, H, N), torch.float32)
+    fa.fwd(q, k, v, scale, causal, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    assert h.guards_intact(ob) and h.guards_intact(lb), "write outside O/LSE"
+    assert torch.isfinite(o.float()).all(), "unwritten or non-finite O"
+    assert torch.isfinite(lse).all(), "unwritten or non-finite LSE"
+    return h.np64(o), h.np64(lse)
+
+
+def test_f32_single_head_workload():
+    w = inputs.WORKLOADS["single_head_f32"]
+    x = inputs.workload_inputs(w)
+    o, lse = run_fwd(x, w.scale, False)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), w.scale, False)
+    assert h.max_abs(o, O) <= h.TOL_F32
+    assert h.max_abs(lse, L) <= h.TOL_F32
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_worked_3x2_example(dtype):
+    """The 3x2 example of "Flash Attention, From First Principles" (scale 1),
+    zero-padded to d = 64 so that the scores are unchanged."""
+    g = load_golden("fp_3x2_example.json")
+    Q = torch.zeros((1, 1, 3, 64))
+    K = torch.zeros((1, 1, 3, 64))
+    V = torch.zeros((1, 1, 3, 64))
+    Q[0, 0, :, :2] = torch.tensor(g["Q"], dtype=torch.float32)
+    K[0, 0, :, :2] = torch.tensor(g["K"], dtype=torch.float32)
+    V[0, 0, :, :2] = torch.tensor(g["V"], dtype=torch.float32)
+    cast = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = {"Q": Q.to(cast), "K": K.to(cast), "V": V.to(cast)}
+    o, lse = run_fwd(x, 1.0, False)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 1.0)
+    tol_o = h.TOL_F32 if dtype == "f32" else h.TOL_O_BF16
+    tol_l = h.TOL_F32 if dtype == "f32" else h.TOL_LSE_BF16
+    assert h.max_abs(o, O) <= tol_o
+    assert h.max_abs(lse, L) <= tol_l
+    assert np.max(np.abs(o[0, 0, :, :2] - np.array(g["O"]))) <= 5e-4 + tol_o
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 255, 256, 300, 513])
+def test_bf16_small_ragged(N, d, causal):
+    x = h.seeded(2, 2, N, d, seed=100 + N + d, dtype="bf16")
+    sc = d ** -0.5
+    o, lse = run_fwd(x, sc, causal)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), sc, causal)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [64, 200, 320])
+def test_f32_small_ragged(N, causal):
+    x = h.seeded(1, 3, N, 128, seed=300 + N, dtype="f32")
+    o, lse = run_fwd(x, 0.125, causal)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 0.125, causal)
+    assert h.max_abs(o, O) <= h.TOL_F32
+    assert h.max_abs(lse, L) <= h.TOL_F32
+
+
+def test_bf16_later_block_holds_the_max():
+    """"FlashAttention from scratch" test recipe: the largest score of every
+    row sits in the last key block, so every row rescales."""
+    N, d = 640, 128
+    x = h.seeded(1, 2, N, d, seed=77, dtype="bf16")
+    K = x["K"].float()
+    K[:, :, -100:, :] *= 3.0
+    x["K"] = K.to(torch.bfloat16)
+    o, lse = run_fwd(x, d ** -0.5, False)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), d ** -0.5)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+def test_bf16_large_logits_stay_finite():
+    """Logits with a range near 58 ("LLM Architecture Refresh [3]",
+    section 3): no overflow, no NaN."""
+    N, d = 512, 64
+    x = h.seeded(1, 2, N, d, seed=78, dtype="bf16")
+    o, lse = run_fwd(x, 1.0, True)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 1.0, True)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+def _sampled_parity(w, causal, per_head=48):
+    x = inputs.workload_inputs(w, with_dO=False)
+    o, lse = run_fwd(x, w.scale, causal)
+    rows = inputs.sample_rows(w.B, w.H, w.N, per_head=per_head, seed=w.seed).numpy()
+    Q, K, V = (inputs.to_f64(x[n]) for n in ("Q", "K", "V"))
+    O, L = oracle.fwd_rows(Q, K, V, w.scale, causal, rows)
+    og = o.reshape(-1, w.d)[rows]
+    lg = lse.reshape(-1)[rows]
+    return h.max_abs(og, O), h.max_abs(lg, L)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("name", ["gpt2_medium_fwd", "llama3_8b_fwd"])
+def test_workload_full_size_sampled(name, causal):
+    eo, el = _sampled_parity(inputs.WORKLOADS[name], causal)
+    assert eo <= h.TOL_O_BF16 and el <= h.TOL_LSE_BF16, (eo, el)
+
+
+@pytest.mark.parametrize("name", ["long_ctx_8k", "long_ctx_16k", "long_ctx_32k"])
+def test_long_context_sampled(name):
+    eo, el = _sampled_parity(inputs.WORKLOADS[name], True, per_head=24)
+    assert eo <= h.TOL_O_BF16 and el <= h.TOL_LSE_BF16, (eo, el)
+
+
+def test_repeated_calls_are_identical():
+    x = h.seeded(2, 4, 777, 128, seed=5, dtype="bf16")
+    a = run_fwd(x, 0.1, True)
+    b = run_fwd(x, 0.1, True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_bounded_wait_times_out_and_reports():
+    """Failure detection without a fault: a wait on a barrier that nothing
+    completes gives up after 0.2 s, and the host reads FA_ERR_TIMEOUT."""
+    assert fa.fa_selftest_wait_timeout(200000, None) == fa.FA_OK
+    assert fa.last_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.last_device_status() == fa.FA_OK  # cleared by the read
+    x = h.seeded(1, 1, 256, 64, seed=6, dtype="bf16")
+    run_fwd(x, 0.125, False)  # the context is still usable

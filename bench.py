@@ -1,0 +1,417 @@
+"""Benchmark: exact tiled attention on GB300, one JSON line on stdout.
+
+A step is one pass of the whole hot path over one batch: fa_fwd then fa_bwd
+(schedule, TMA loads, S = QK^T, masking, online softmax, PV, epilogue; then
+D, recompute of S and P, dV, dP, dS, dK, dQ and the dQ conversion) on the
+training workload: B=8, H=16, N=2048, d=128, bf16, causal, synthetic
+iid N(0,1) inputs (seeded).  The metric is attention TFLOP/s counted the
+pages' way: 4*N^2*d per head for the forward, 14*N^2*d for forward+backward
+(the backward's five matmuls), halved under the causal mask.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`value` is device-timed (inputs resident in HBM; every input tensor is
+larger than L2, so no flush is needed between steps); `e2e` times the same
+step through the public API with pinned host buffers, copies included;
+`fwd` holds forward-only TFLOP/s of the Llama-3.1-8B-shaped and long-context
+workloads.  `--impl reference` times the fp64 CPU oracle (the only other
+implementation of this computation) on a bounded sample of the same
+workload on the host cores.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd at 1 GB300; % of dense BF16 tensor peak"
+WORKLOAD = "train_fwd_bwd"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def attn_flops(B, H, N, d, causal, passes):
+    per_head = (4 if passes == "fwd" else 14) * N * N * d
+    if causal:
+        per_head /= 2
+    return per_head * B * H
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def profile_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if the
+    summary was taken on the current kernel sources; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "exact_tiled_attention_sm_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    try:
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel_key and parts[2] == digest:
+                return float(parts[1])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed regions run."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sms, maxs, reasons, n = [], [], set(), 0
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, mx, pw = float(parts[0]), float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            n += 1
+            maxs.append(mx)
+            if pw > 250:  # under load
+                sms.append(sm)
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        sms.sort()
+        med = sms[len(sms) // 2] if sms else None
+        return {"sm_mhz": med, "sm_max_mhz": max(maxs) if maxs else None,
+                "reasons": sorted(reasons), "samples": n, "samples_under_load": len(sms)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    import torch
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    import torch
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+    import exact_tiled_attention_sm_gb300 as fa
+    from exact_tiled_attention_sm_gb300 import inputs
+
+    world, rank, local = dist_setup()
+    w = inputs.WORKLOADS[WORKLOAD]
+    B, H, N, d, sc = w.B, w.H, w.N, w.d, w.scale
+    causal = True
+    stream = torch.cuda.current_stream()
+    host = inputs.workload_inputs(w)  # every rank: its own replica of the batch
+    q, k, v, do = (host[n].cuda() for n in ("Q", "K", "V", "dO"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.workspace(B, H, N, d)
+
+    def step():
+        fa.fwd(q, k, v, sc, causal, out=o, lse=lse)
+        fa.bwd(q, k, v, o, do, lse, sc, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = fa.last_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after warm-up: {fa.status_string(st)}")
+
+    sampler.start()
+    time.sleep(0.3)
+    # --- device-timed region: K steps, per-call events on the launch stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fa.fwd(q, k, v, sc, causal, out=o, lse=lse)
+        ev[i][1].record(stream)
+        fa.bwd(q, k, v, o, do, lse, sc, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    barrier(world)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / args.steps
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in ev) / args.steps
+    launches = args.steps * (1 + 3)  # fwd kernel; bwd pre, main, convert
+
+    # --- e2e: pinned host buffers -> device -> fwd + bwd -> host, per step
+    pin = {n: host[n].pin_memory() for n in ("Q", "K", "V", "dO")}
+    outs = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=True)
+            for n in ("O", "dQ", "dK", "dV")}
+    lse_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values()) + lse_h.numel() * 4
+
+    def e2e_step():
+        q.copy_(pin["Q"], non_blocking=True)
+        k.copy_(pin["K"], non_blocking=True)
+        v.copy_(pin["V"], non_blocking=True)
+        do.copy_(pin["dO"], non_blocking=True)
+        step()
+        outs["O"].copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        outs["dQ"].copy_(dq, non_blocking=True)
+        outs["dK"].copy_(dk, non_blocking=True)
+        outs["dV"].copy_(dv, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 4)
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+
+    # --- forward-only workloads (the forward metric), each timed on its own
+    fwd_results = {}
+    for name, causal_list in (("llama3_8b_fwd", (False, True)), ("long_ctx_32k", (True,))):
+        wf = inputs.WORKLOADS[name]
+        xf = inputs.workload_inputs(wf, with_dO=False)
+        qf, kf, vf = (xf[n].cuda() for n in ("Q", "K", "V"))
+        of = torch.empty_like(qf)
+        lf = torch.empty((wf.B, wf.H, wf.N), dtype=torch.float32, device="cuda")
+        for c in causal_list:
+            reps = max(5, args.steps // 2)
+            for _ in range(3):
+                fa.fwd(qf, kf, vf, wf.scale, c, out=of, lse=lf)
+            barrier(world)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fa.fwd(qf, kf, vf, wf.scale, c, out=of, lse=lf)
+            b.record(stream)
+            barrier(world)
+            ms = max_over_ranks(a.elapsed_time(b), world) / reps
+            fl = attn_flops(wf.B, wf.H, wf.N, wf.d, c, "fwd")
+            key = f"{name}{'_causal' if c else ''}"
+            fwd_results[key] = {"tflops": round(world * fl / (ms * 1e-3) / 1e12, 1),
+                                "ms": round(ms, 4), "launches": reps}
+            launches += reps
+        del qf, kf, vf, of, lf
+    clocks = sampler.stop()
+    st = fa.last_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status after timing: {fa.status_string(st)}")
+
+    if rank != 0:
+        return None
+    peak, peak_sustained, peak_src = measured_peaks()
+    step_flops = attn_flops(B, H, N, d, causal, "fwd+bwd")
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    bwd_flops = step_flops - attn_flops(B, H, N, d, causal, "fwd")
+    bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = attn_flops(B, H, N, d, causal, "fwd") / (fwd_ms * 1e-3) / 1e12
+    for r in fwd_results.values():
+        r["frac_of_peak"] = round(r["tflops"] / world / peak, 4)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded iid N(0,1) bf16 tensors of the workload's shape",
+        "config": {"workload": "train_fwd_bwd: B=8 H=16 N=2048 d=128 bf16 causal, fa_fwd + fa_bwd",
+                   "B": B, "H": H, "N": N, "d": d, "causal": True, "scale": sc,
+                   "parallelism": f"replicas x{world} (heads independent; no collective)",
+                   "l2": "no flush: inputs larger than L2 (Q, K, V, dO, O are 64 MiB each; 320 MiB read per step)"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "fa_bwd call (bwd_pre + bwd_kernel<128> + dq_convert launches)",
+            "achieved": round(bwd_tflops, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+            "unit": "TFLOP/s",
+            "frac": round(bwd_tflops / peak, 4),
+            "traffic": profile_traffic("bwd_kernel_train"),
+            "algorithmic_flops_per_launch": bwd_flops,
+        },
+        "roofline_fwd": {
+            "bound": "tensor",
+            "kernel": "fwd_kernel<128> (one launch per fa_fwd)",
+            "achieved": round(fwd_tflops, 1),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(fwd_tflops / peak, 4),
+            "traffic": profile_traffic("fwd_kernel_train"),
+            "algorithmic_flops_per_launch": attn_flops(B, H, N, d, causal, "fwd"),
+        },
+        "fwd": fwd_results,
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------- the oracle on CPU
+def oracle_sample_step(w, heads, nthreads):
+    """One bounded sample of the workload through the fp64 oracle: forward
+    and backward of `heads` whole heads, one head per host thread."""
+    import numpy as np
+    import oracle
+    from exact_tiled_attention_sm_gb300 import inputs
+    x = inputs.seeded_inputs(1, heads, w.N, w.d, w.seed, w.dtype, with_dO=True)
+    Q, K, V, dO = (inputs.to_f64(x[n]) for n in ("Q", "K", "V", "dO"))
+    t = time.perf_counter()
+    oracle.fwd(Q, K, V, w.scale, True, nthreads=nthreads)
+    oracle.bwd(Q, K, V, dO, w.scale, True, nthreads=nthreads)
+    return time.perf_counter() - t, attn_flops(1, heads, w.N, w.d, True, "fwd+bwd")
+
+
+def cpu_baseline(w, budget_s=15.0):
+    """The oracle on the host cores: a first batch of one head per core sizes
+    the sample so that the timed batch takes about `budget_s` seconds (at most
+    the whole workload)."""
+    import oracle
+    cores = oracle.cores()
+    t1, _ = oracle_sample_step(w, cores, cores)
+    total = w.B * w.H
+    heads = max(cores, int(cores * budget_s / max(t1, 1e-3)) // cores * cores)
+    heads = min(heads, total)
+    secs, flops = oracle_sample_step(w, heads, cores)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{heads} of the {total} heads of {w.name} (N={w.N}, d={w.d}, causal), "
+                      f"fp64 forward + backward, one head per thread at a time, {secs:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    from exact_tiled_attention_sm_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD]
+    cores = oracle.cores()
+    heads = cores
+    for _ in range(args.warmup):
+        oracle_sample_step(w, heads, cores)
+    tot_s, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_sample_step(w, heads, cores)
+        tot_s += s
+        tot_f += f
+    value = tot_f / tot_s / 1e12
+    sample = (f"{heads} of the {w.B * w.H} heads of {w.name} per step (N={w.N}, d={w.d}, "
+              f"causal), fp64 forward + backward, one head per host thread")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic: seeded iid N(0,1), rounded to bf16, widened to fp64",
+        "config": {"workload": "train_fwd_bwd: B=8 H=16 N=2048 d=128 bf16 causal, fa_fwd + fa_bwd",
+                   "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -17,7 +17,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 FA_BF16, FA_F32 = 0, 1
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_last_device_status",
+EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
+           "fa_last_device_status",
            "fa_status_string", "fa_selftest_wait_timeout",
            "fa_fwd_schedule_census", "fa_version")
 
@@ -47,6 +48,9 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
                              i, i, vp, ctypes.c_size_t, vp]
         L.fa_bwd.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i,
+                                     i, i, f, i, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_last_device_status.argtypes = [vp]
         L.fa_last_device_status.restype = i
         L.fa_status_string.argtypes = [i]
@@ -74,6 +78,14 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, dt,
            workspace, workspace_bytes, stream):
     return lib().fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale,
                         int(causal), dt, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
+                   dt, stream):
+    """fa_bwd with the library's own scratch array instead of a workspace, for
+    callers that cannot allocate device memory (see include/fa.h)."""
+    return lib().fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d,
+                                scale, int(causal), dt, stream)
 
 
 def fa_last_device_status(stream=None):

@@ -84,6 +84,38 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
                  int causal, fa_dtype dt, void* workspace,
                  size_t workspace_bytes, void* stream);
 
+/* Size of the device scratch array that fa_bwd_noalloc uses in place of a
+ * caller workspace: 64 MiB, statically reserved on every GPU that loads the
+ * library (the reservation lasts until the process exits). */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* The backward pass for callers that cannot allocate device memory.  Some
+ * callers only ever receive input and output buffers and have no way to
+ * obtain more: a plugin whose host framework owns every device allocation
+ * and hands out no allocator, a latency-critical loop where the implicit
+ * synchronisation of cudaMalloc is not acceptable, or a deployment with a
+ * device-memory budget fixed up front.  This entry point takes the
+ * same arguments as fa_bwd minus the workspace and uses a
+ * FA_BWD_NOALLOC_SCRATCH_BYTES array owned by the library instead; it calls
+ * no cudaMalloc, cudaFree or other allocating routine.  (The pages have no
+ * counterpart of this entry point: it is plumbing of this library.)
+ *   - Sizes whose fa_bwd_workspace_size() exceeds the scratch are rejected
+ *     with FA_ERR_INVALID_ARG before anything is launched (for d = 128 that
+ *     is B*H*N above about 130,000 rows: 32 heads of 2048 fit, 32 of 4096 do
+ *     not).  Other argument errors are those of fa_bwd.
+ *   - The first call on a device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress, with that device current) and
+ *     keeps it; make that first call before any stream capture.
+ *   - All calls in the process share the one array and it keeps the last
+ *     call's contents; the backward clears what must start at zero itself.
+ *     Calls that overlap on the GPU (different streams, or several host
+ *     threads) race on the array: serialise them. */
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V,
+                         const void* O, const void* dO, const float* LSE,
+                         void* dQ, void* dK, void* dV, int B, int H, int N,
+                         int d, float scale, int causal, fa_dtype dt,
+                         void* stream);
+
 /* Synchronises `stream`, then returns and clears the device-side status of
  * this library's kernels on the current device: FA_OK, or FA_ERR_TIMEOUT if
  * a bounded wait ran out since the last call (the kernel that gave up

@@ -151,6 +151,37 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+# ------------------------------------------------------------------ profile
+def run_profile(args):
+    """Only the launches of one workload (for ncu): W warm-up steps then K
+    steps, nothing else on the GPU.  `train_fwd_bwd` runs fa_fwd + fa_bwd
+    (4 launches a step); a forward workload runs fa_fwd (1 launch a step)."""
+    import torch
+    import exact_tiled_attention_sm_gb300 as fa
+    from exact_tiled_attention_sm_gb300 import inputs
+    torch.cuda.set_device(0)
+    w = inputs.WORKLOADS[args.workload]
+    x = inputs.workload_inputs(w)
+    q, k, v = (x[n].cuda() for n in ("Q", "K", "V"))
+    causal = args.causal if w.passes == "fwd" else True
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    if w.passes == "fwd+bwd":
+        do = x["dO"].cuda()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = fa.workspace(w.B, w.H, w.N, w.d)
+    for _ in range(args.warmup + args.steps):
+        fa.fwd(q, k, v, w.scale, causal, out=o, lse=lse)
+        if w.passes == "fwd+bwd":
+            fa.bwd(q, k, v, o, do, lse, w.scale, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+    torch.cuda.synchronize()
+    st = fa.last_device_status()
+    if st != fa.FA_OK:
+        raise SystemExit(f"device status: {fa.status_string(st)}")
+    return {"profile": args.workload, "causal": causal, "steps": args.steps,
+            "warmup": args.warmup}
+
+
 # --------------------------------------------------------------------- ours
 def run_ours(args):
     import torch
@@ -406,9 +437,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="run only --workload's launches (for ncu captures)")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--causal", type=int, default=1)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.profile:
+        line = run_profile(args)
+    elif args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -84,6 +84,22 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// fp32 [B*H, N, d] dQ accumulator; boxes of 32 columns x 32 rows x 1 head,
+// 128-byte swizzle; used only as the target of bulk reduce-adds.
+fa_status make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 bool aligned16(const void* p) {
   return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
@@ -182,6 +198,7 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
   if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.dO, dO, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map_f32(&maps.dq_acc, dQacc, BH, N, d)) != FA_OK) return st;
   if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, dQacc, cs))) !=
       FA_OK)
     return st;

@@ -11,19 +11,24 @@
 // 128 keys, whose K and V tiles stay resident in shared memory while the
 // query blocks i stream past (K/V-outer order, so dK and dV accumulate in
 // TMEM and are written once).  Per query block the tensor core computes the
-// transposed tiles S^T = K Q_i^T and dP^T = V dO_i^T (rows = keys), the dS
-// warpgroup turns them into P^T and scale*dS^T, and the tensor core then
-// forms dV += P^T dO_i and dK += dS^T Q_i (P^T and dS^T read straight from
-// TMEM) and dQ_i = dS K (dS read from shared memory); the dQ warpgroup adds
-// dQ_i into the fp32 accumulator with vector atomics.
+// transposed tiles S^T = K Q_i^T and dP^T = V dO_i^T (rows = keys); two
+// warpgroups (64 query columns each) turn S^T into P^T while the tensor core
+// still computes dP^T, then turn dP^T into scale*dS^T while it already forms
+// dV += P^T dO_i; then dK += dS^T Q_i (P^T and dS^T read straight from TMEM)
+// and dQ_i = dS K (dS read from shared memory).  dQ_i is
+// copied out of TMEM into the just-consumed Q_i / dO_i stage and added into
+// the fp32 dQ accumulator in global memory with TMA bulk reduce-adds, so the
+// tensor memory is free again as soon as it has been read.
 //
-// Roles: warps 0-3 dS (one thread per key row), warps 4-7 dQ atomics and the
-// dK/dV epilogue, warp 8 tensor-core issuer and TMEM owner, warp 9 loads
-// (TMA for K, V, Q, dO; plain loads for LSE and D).
+// Roles: warps 0-3 dS for query columns 0-63 and the dV epilogue; warps 4-7
+// dS for columns 64-127, the dQ reduction and the dK epilogue; warp 8
+// tensor-core issuer and TMEM owner; warp 9 loads (TMA for K, V, Q, dO;
+// plain loads for LSE and D).
 //
-// TMEM: S^T [0,128) (P^T aliases its first 64 columns), dP^T [128,256) (dS^T
-// aliases its first 64 columns, and dQ_i reuses the block once dK has read
-// dS^T), dV [256, 256+d), dK [256+d, 256+2d).
+// TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+d), dK [256+d, 256+2d).
+// P^T overwrites columns [0,32) (queries 0-63) and [64,96) (queries 64-127)
+// of S^T, each half inside the columns its own warpgroup has already read;
+// dS^T likewise inside dP^T; dQ_i then reuses the dP^T columns.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -44,12 +49,14 @@ struct Cfg {
   static constexpr int OFF_DO = OFF_Q + QST * TILE_BYTES;
   static constexpr int OFF_DS = OFF_DO + QST * TILE_BYTES;   // dS^T [128][128]
   static constexpr int OFF_STAT = OFF_DS + 2 * kChunkBytes;  // per stage
-  static constexpr int STAT_BYTES = 2 * 128 * 4;             // lse2[128], D[128]
+  static constexpr int STAT_BYTES = 2 * 128 * 4;  // LSE*log2(e)[128], D*scale[128]
   static constexpr int OFF_BAR = OFF_STAT + QST * STAT_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
   static constexpr int B_QFULL = 2, B_QEMPTY = B_QFULL + QST;
-  static constexpr int B_SDP = B_QEMPTY + QST;
-  static constexpr int B_DSREADY = B_SDP + 1;
+  static constexpr int B_SFULL = B_QEMPTY + QST;   // S^T in TMEM
+  static constexpr int B_DPFULL = B_SFULL + 1;      // dP^T in TMEM
+  static constexpr int B_PREADY = B_DPFULL + 1;     // P^T written
+  static constexpr int B_DSREADY = B_PREADY + 1;    // dS^T written
   static constexpr int B_DQFULL = B_DSREADY + 1;
   static constexpr int B_DQFREE = B_DQFULL + 1;
   static constexpr int B_DKDVDONE = B_DQFREE + 1;
@@ -73,7 +80,6 @@ constexpr int kLoadWarp = 9;
 struct Params {
   const float* LSE;
   const float* Dvec;
-  float* dQacc;
   __nv_bfloat16* dK;
   __nv_bfloat16* dV;
   float scale;
@@ -84,16 +90,112 @@ struct Params {
 
 enum : uint32_t {
   SITE_L_KVEMPTY = 1, SITE_L_QEMPTY, SITE_M_KVFULL, SITE_M_QFULL, SITE_M_DQFREE,
-  SITE_M_DSREADY, SITE_M_DKDVFREE, SITE_S_QFULL, SITE_S_SDP, SITE_Q_DQFULL,
-  SITE_Q_DKDVDONE, SITE_DRAIN, SITE_ALIGN
+  SITE_M_DSREADY, SITE_M_DKDVFREE, SITE_S_QFULL, SITE_S_SFULL, SITE_Q_DQFULL,
+  SITE_E_DKDVDONE, SITE_DRAIN, SITE_ALIGN, SITE_M_PREADY, SITE_S_DPFULL
 };
+
+// One warpgroup's half of the softmax-gradient step for query block i:
+// chunks c0, c0+1 of 32 query columns; thread = key row r (TMEM lane).
+// Phase P (needs only S^T): P^T = 2^(S*scale*log2(e) - LSE*log2(e)), kept in
+// fp32 registers and written to TMEM as bf16 at `pcol` (columns relative to
+// the S^T block, inside the columns this warpgroup has read).
+__device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
+                                       const float* lse2, int c0, uint32_t pcol,
+                                       int key, bool kvalid, bool diag, int q0,
+                                       float sl2, float (&pr)[64]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = c0 + h;
+    uint32_t sr[32];
+    tmem_ld32(tmem_row + tm_s + 32 * c, sr);
+    tmem_ld_wait();
+    reg_fence32(sr);
+    const float4* l4 = reinterpret_cast<const float4*>(lse2 + 32 * c);
+    uint32_t pp[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 lv = l4[e / 4];
+      const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float v = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -la[u]));
+        if (diag && q0 + 32 * c + e + u < key) v = 0.f;
+        if (!kvalid) v = 0.f;
+        pr[32 * h + e + u] = v;
+      }
+      pp[e / 2] = pack_bf16x2(pr[32 * h + e], pr[32 * h + e + 1]);
+      pp[e / 2 + 1] = pack_bf16x2(pr[32 * h + e + 2], pr[32 * h + e + 3]);
+    }
+    tmem_st16(tmem_row + tm_s + pcol + 16 * h, pp);
+  }
+}
+
+// Phase dS (needs dP^T): scale*dS^T = P * (dP*scale - D*scale), written to
+// TMEM at `pcol` of the dP^T block and to the swizzled shared tile.
+template <int D>
+__device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
+                                        const float* dsc, int c0, uint32_t pcol,
+                                        int r, float scale,
+                                        const float (&pr)[64]) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = c0 + h;
+    uint32_t dr[32];
+    tmem_ld32(tmem_row + C::TM_DP + 32 * c, dr);
+    tmem_ld_wait();
+    reg_fence32(dr);
+    const float4* d4 = reinterpret_cast<const float4*>(dsc + 32 * c);
+    uint32_t dd[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 dv = d4[e / 4];
+      const float da[4] = {dv.x, dv.y, dv.z, dv.w};
+      float ds[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        ds[u] = pr[32 * h + e + u] * fmaf(__uint_as_float(dr[e + u]), scale, -da[u]);
+      dd[e / 2] = pack_bf16x2(ds[0], ds[1]);
+      dd[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+    }
+    tmem_st16(tmem_row + C::TM_DP + pcol + 16 * h, dd);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(smem + C::OFF_DS + swz_offset(r, 4 * c + k)) =
+          make_uint4(dd[4 * k], dd[4 * k + 1], dd[4 * k + 2], dd[4 * k + 3]);
+  }
+}
+
+// Reads one 128 x D fp32 accumulator (lanes = rows) and stores row r as bf16.
+template <int D>
+__device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
+                                                __nv_bfloat16* out, bool store) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tmem_col + 32 * c, v);
+    tmem_ld_wait();
+    reg_fence32(v);
+    uint4 o[4];
+    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      ow[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[k] = o[k];
+    }
+  }
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv,
-               const __grid_constant__ CUtensorMap mdo, const Params p) {
+               const __grid_constant__ CUtensorMap mdo,
+               const __grid_constant__ CUtensorMap mdq, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
@@ -117,14 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_KVEMPTY), 1);
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1 + 32);  // TMA arrive + 32 stat writers
-      mbar_init(bar(C::B_QEMPTY + s), 1);
+      mbar_init(bar(C::B_QEMPTY + s), 4);      // the 4 dQ-reduction warps
     }
-    mbar_init(bar(C::B_SDP), 1);
-    mbar_init(bar(C::B_DSREADY), 128);
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_PREADY), 256);
+    mbar_init(bar(C::B_DSREADY), 256);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 128);
     mbar_init(bar(C::B_DKDVDONE), 1);
-    mbar_init(bar(C::B_DKDVFREE), 128);
+    mbar_init(bar(C::B_DKDVFREE), 256);
     mbar_init(bar(C::B_MMADONE), 1);
     *abort_flag = 0;
     if (sb & 1023u) record_timeout(abort_flag, SITE_ALIGN);
@@ -178,8 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // LSE (as log2) and D of the block's 128 queries; rows past N get
-        // LSE = +inf so that their P is exactly 0
+        // LSE*log2(e) and D*scale of the block's 128 queries; rows past N
+        // get LSE = +inf so that their P is exactly 0
         float* st = stat(s);
         const size_t base = (size_t)bh * N;
 #pragma unroll
@@ -188,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int q = i * 128 + qi;
           const bool valid = q < N;
           st[qi] = valid ? p.LSE[base + q] * 1.4426950408889634f : INFINITY;
-          st[128 + qi] = valid ? p.Dvec[base + q] : 0.f;
+          st[128 + qi] = valid ? p.Dvec[base + q] * p.scale : 0.f;
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES);
@@ -241,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           mma_rows_x_rows<D>(tmem + C::TM_S, sK, sQ(s), C::IDESC_SS);
-          if (g > 0) {  // dQ of the previous block has been read out
+          umma_commit(bar(C::B_SFULL));
+          if (g > 0) {  // dQ of the previous block has left TMEM
             if (!wait_one(bar(C::B_DQFREE), (g - 1) & 1, abort_flag, lim,
                           SITE_M_DQFREE)) {
               ok = false;
@@ -250,9 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           mma_rows_x_rows<D>(tmem + C::TM_DP, sV, sdO(s), C::IDESC_SS);
-          umma_commit(bar(C::B_SDP));
-          if (!wait_one(bar(C::B_DSREADY), g & 1, abort_flag, lim,
-                        SITE_M_DSREADY)) {
+          umma_commit(bar(C::B_DPFULL));
+          if (!wait_one(bar(C::B_PREADY), g & 1, abort_flag, lim,
+                        SITE_M_PREADY)) {
             ok = false;
             break;
           }
@@ -266,14 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
           }
-          mma_tmem_x_rows(tmem + C::TM_DV, tmem + C::TM_S, sdO(s), C::IDESC_TS,
-                          !first);
-          mma_tmem_x_rows(tmem + C::TM_DK, tmem + C::TM_DP, sQ(s), C::IDESC_TS,
-                          !first);
-          umma_commit(bar(C::B_QEMPTY + s));
-          ++qcnt;
+          mma_tmem2_x_rows(tmem + C::TM_DV, tmem + C::TM_S, tmem + C::TM_S + 64,
+                           sdO(s), C::IDESC_TS, !first);
+          if (!wait_one(bar(C::B_DSREADY), g & 1, abort_flag, lim,
+                        SITE_M_DSREADY)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_tmem2_x_rows(tmem + C::TM_DK, tmem + C::TM_DP,
+                           tmem + C::TM_DP + 64, sQ(s), C::IDESC_TS, !first);
           mma_colsT_x_rows(tmem + C::TM_DP, sDS, sK, C::IDESC_DQ);
           umma_commit(bar(C::B_DQFULL));
+          ++qcnt;
           ++g;
         }
         if (!ok) break;
@@ -286,12 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_one(bar(C::B_MMADONE), 0, &no_abort, lim, SITE_DRAIN);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------- dS
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int r = warp * 32 + lane;  // key row within the block
+  } else {
+    // ------------------------------------- dS (both warpgroups), dQ, dK, dV
+    const int grp = warp >> 2;        // 0: query columns 0-63, 1: 64-127
+    const int wq = warp & 3;          // TMEM lane quarter
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tmem_row = tmem + lane_off;
+    const int r = wq * 32 + lane;     // key row (dS, dK, dV) / query row (dQ)
     const float sl2 = p.scale_log2, scale = p.scale;
-    uint32_t qcnt = 0, g = 0;
+    uint32_t qcnt = 0, g = 0, it = 0;
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
@@ -304,131 +417,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = qcnt % C::QST;
         if (!wait_warp(bar(C::B_QFULL + s), (qcnt / C::QST) & 1, abort_flag,
                        lim, SITE_S_QFULL) ||
-            !wait_warp(bar(C::B_SDP), g & 1, abort_flag, lim, SITE_S_SDP)) {
+            !wait_warp(bar(C::B_SFULL), g & 1, abort_flag, lim, SITE_S_SFULL)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const float* lse2 = stat(s);
-        const float* dvec = lse2 + 128;
         const int q0 = i * 128;
         const bool diag = sc.causal && i == kb;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32], dr[32];
-          tmem_ld32(tmem + lane_off + C::TM_S + 32 * c, sr);
-          tmem_ld32(tmem + lane_off + C::TM_DP + 32 * c, dr);
-          tmem_ld_wait();
-          reg_fence32(sr);
-          reg_fence32(dr);
-          uint32_t pp[16], dd[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = 32 * c + e + u;
-              float pr = ex2_approx(__uint_as_float(sr[e + u]) * sl2 - lse2[qi]);
-              if (!kvalid || (diag && q0 + qi < key)) pr = 0.f;
-              pv[u] = pr;
-              dv[u] = pr * (__uint_as_float(dr[e + u]) - dvec[qi]) * scale;
-            }
-            pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-            dd[e / 2] = pack_bf16x2(dv[0], dv[1]);
-          }
-          tmem_st16(tmem + lane_off + C::TM_S + 16 * c, pp);
-          tmem_st16(tmem + lane_off + C::TM_DP + 16 * c, dd);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v = make_uint4(dd[4 * k], dd[4 * k + 1], dd[4 * k + 2],
-                                 dd[4 * k + 3]);
-            *reinterpret_cast<uint4*>(smem + C::OFF_DS + swz_offset(r, 4 * c + k)) = v;
-          }
-        }
+        float pr[64];
+        p_half(tmem_row, C::TM_S, lse2, 2 * grp, 64u * grp, key, kvalid, diag,
+               q0, sl2, pr);
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(C::B_DSREADY));
-        ++qcnt;
-        ++g;
-      }
-    }
-  } else {
-    // ------------------------------------------------- dQ atomics, dK / dV
-    const int wq = warp - 4;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int r = wq * 32 + lane;
-    uint32_t g = 0, it = 0;
-    bool ok = true;
-    for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
-      const int item = sc.item_of(blockIdx.x, w);
-      if (item < 0) continue;
-      int bh, kb;
-      sc.decode(item, bh, kb);
-      for (int i = sc.q_begin(kb); i < sc.n_blk; ++i) {
-        if (!wait_warp(bar(C::B_DQFULL), g & 1, abort_flag, lim, SITE_Q_DQFULL)) {
+        mbar_arrive(bar(C::B_PREADY));
+        if (!wait_warp(bar(C::B_DPFULL), g & 1, abort_flag, lim, SITE_S_DPFULL)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const int q = i * 128 + r;
-        float4* dst = reinterpret_cast<float4*>(
-            p.dQacc + ((size_t)bh * N + (size_t)(q < N ? q : 0)) * D);
+        ds_half<D>(tmem_row, smem, lse2 + 128, 2 * grp, 64u * grp, r, scale, pr);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSREADY));
+        if (grp == 1) {
+          // dQ_i: TMEM -> swizzled fp32 staging in the consumed Q/dO stage ->
+          // bulk reduce-add into the accumulator, 32 rows per warp
+          if (!wait_warp(bar(C::B_DQFULL), g & 1, abort_flag, lim,
+                         SITE_Q_DQFULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::TM_DP + 32 * c, v);
-          tmem_ld_wait();
-          reg_fence32(v);
-          if (q < N) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem_row + C::TM_DP + 32 * c, v);
+            tmem_ld_wait();
+            reg_fence32(v);
+            const uint32_t base =
+                c < C::CH ? sQ(s) + c * kChunkBytes : sdO(s) + (c - C::CH) * kChunkBytes;
+            uint8_t* row = smem + (base - sb) + r * 128;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              atomicAdd(dst + 8 * c + k,
-                        make_float4(__uint_as_float(v[4 * k]),
-                                    __uint_as_float(v[4 * k + 1]),
-                                    __uint_as_float(v[4 * k + 2]),
-                                    __uint_as_float(v[4 * k + 3])));
+              *reinterpret_cast<uint4*>(row + ((k ^ (r & 7)) << 4)) =
+                  make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
           }
+          tc_fence_before();
+          mbar_arrive(bar(C::B_DQFREE));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int y = q0 + wq * 32;
+            if (y < N) {
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                const uint32_t base = c < C::CH
+                                          ? sQ(s) + c * kChunkBytes
+                                          : sdO(s) + (c - C::CH) * kChunkBytes;
+                tma_reduce_add_3d(&mdq, base + wq * 32 * 128, 32 * c, y, bh);
+              }
+              bulk_commit_group();
+              bulk_wait_group_read0();
+            }
+            mbar_arrive(bar(C::B_QEMPTY + s));
+          }
+          __syncwarp();
         }
-        tc_fence_before();
-        mbar_arrive(bar(C::B_DQFREE));
+        ++qcnt;
         ++g;
       }
       if (!ok) break;
       if (!wait_warp(bar(C::B_DKDVDONE), it & 1, abort_flag, lim,
-                     SITE_Q_DKDVDONE))
+                     SITE_E_DKDVDONE))
         break;
       tc_fence_after();
-      const int key = kb * 128 + r;
       const bool store = key < N;
-      const size_t row = ((size_t)bh * N + (size_t)(store ? key : 0)) * D;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = (which == 0 ? p.dV : p.dK) + row;
-        const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + col + 32 * c, v);
-          tmem_ld_wait();
-          reg_fence32(v);
-          uint4 o[4];
-          uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-          for (int k = 0; k < 16; ++k)
-            ow[k] = pack_bf16x2(__uint_as_float(v[2 * k]),
-                                __uint_as_float(v[2 * k + 1]));
-          if (store) {
-            uint4* dstv = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) dstv[k] = o[k];
-          }
-        }
-      }
+      const size_t rowoff = ((size_t)bh * N + (size_t)(store ? key : 0)) * D;
+      if (grp == 0)
+        store_rows_bf16<D>(tmem_row + C::TM_DV, p.dV + rowoff, store);
+      else
+        store_rows_bf16<D>(tmem_row + C::TM_DK, p.dK + rowoff, store);
       tc_fence_before();
       mbar_arrive(bar(C::B_DKDVFREE));
       ++it;
     }
+    if (grp == 1 && lane == 0) bulk_wait_group0();  // reductions complete
   }
 
   tc_fence_before();
@@ -439,8 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
-                   const float* Dvec, float* dQacc, void* dK, void* dV,
-                   int num_sms, uint64_t lim, cudaStream_t stream) {
+                   const float* Dvec, void* dK, void* dV, int num_sms,
+                   uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D>;
   static cudaError_t attr = cudaFuncSetAttribute(
       bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -448,7 +523,6 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   Params p;
   p.LSE = LSE;
   p.Dvec = Dvec;
-  p.dQacc = dQacc;
   p.dK = reinterpret_cast<__nv_bfloat16*>(dK);
   p.dV = reinterpret_cast<__nv_bfloat16*>(dV);
   p.scale = s.scale;
@@ -459,8 +533,8 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   const int total = BH * n_blk;
   const int grid = total < num_sms ? total : num_sms;
   p.sched.init(BH, s.N, s.causal, grid);
-  bwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v,
-                                                             maps.dO, p);
+  bwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
+      maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, p);
   return cudaGetLastError();
 }
 
@@ -470,11 +544,12 @@ cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
                           const float* LSE, const float* Dvec, float* dQacc,
                           void* dK, void* dV, int num_sms,
                           uint64_t wait_limit_ns, cudaStream_t stream) {
+  (void)dQacc;  // reached through maps.dq_acc
   if (s.d == 64)
-    return bwdtc::launch<64>(s, maps, LSE, Dvec, dQacc, dK, dV, num_sms,
-                             wait_limit_ns, stream);
-  return bwdtc::launch<128>(s, maps, LSE, Dvec, dQacc, dK, dV, num_sms,
-                            wait_limit_ns, stream);
+    return bwdtc::launch<64>(s, maps, LSE, Dvec, dK, dV, num_sms, wait_limit_ns,
+                             stream);
+  return bwdtc::launch<128>(s, maps, LSE, Dvec, dK, dV, num_sms, wait_limit_ns,
+                            stream);
 }
 
 FA_DEFINE_STATUS_READER(read_status_bwd_tc)

@@ -8,15 +8,23 @@
 // Architecture Refresh [3]", section 7), and only the diagonal block (and a
 // ragged last block) is masked element by element.
 //
-// Balance.  Causal items cost in proportion to (pair + 1), so items are
-// listed heaviest first, and a persistent grid takes them in waves of `grid`
-// items with the CTA order reversed on every other wave ("snake"), pairing a
-// heavy item with a light one.  Locality.  The list is grouped by heads:
-// `group` heads at a time, about one wave's worth, so the K/V blocks that a
-// wave's CTAs stream are shared through L2 instead of re-read from HBM.
+// Balance.  Causal items cost in proportion to (pair + 1), so within a group
+// of heads items are listed heaviest first, and a persistent grid takes the
+// list in waves of `grid` items with the CTA order reversed on every other
+// wave ("snake"), pairing heavy with light items.  Locality.  The list is
+// grouped by heads, `group` heads (about kGroupWaves waves of items) at a
+// time, so the K/V blocks that the running CTAs stream are shared through L2
+// instead of re-read from HBM.
 #pragma once
 
 namespace fa {
+
+// Under the causal mask a head group holds about this many waves of items:
+// enough for the snake order to pair heavy with light items within the
+// group, few enough heads that the group's K/V (forward) or Q/dO (backward)
+// stay resident in L2.  Without the mask every item costs the same and one
+// wave per group keeps the most reuse.
+constexpr int kGroupWaves = 4;
 
 struct FwdSched {
   int BH, N, causal, grid;
@@ -30,7 +38,7 @@ struct FwdSched {
     n_q_tiles = (N + 127) / 128;
     n_kv_total = n_q_tiles;
     n_pairs = (n_q_tiles + 1) / 2;
-    int g = grid / n_pairs;
+    int g = (causal ? kGroupWaves : 1) * grid / n_pairs;
     if (g < 1) g = 1;
     if (g > BH) g = BH;
     group = g;
@@ -96,7 +104,7 @@ struct BwdSched {
     causal = is_causal;
     grid = grid_size;
     n_blk = (N + 127) / 128;
-    int g = grid / n_blk;
+    int g = (causal ? kGroupWaves : 1) * grid / n_blk;
     if (g < 1) g = 1;
     if (g > BH) g = BH;
     group = g;

@@ -43,6 +43,19 @@ __device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem
             (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// As mma_tmem_x_rows, with the A operand's 8 column groups (16 K-rows each)
+// split in two halves: groups 0-3 at a_lo + 8*kk, groups 4-7 at
+// a_hi + 8*(kk-4).
+__device__ __forceinline__ void mma_tmem2_x_rows(uint32_t d_tmem, uint32_t a_lo,
+                                                 uint32_t a_hi, uint32_t sb,
+                                                 uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_ts(d_tmem, kk < 4 ? a_lo + kk * 8 : a_hi + (kk - 4) * 8,
+            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
+            (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // D(128 x Dn) = A B with A^T a [128 (K)][128 (M)] tile read MN-major (its
 // two 64-column chunks are the M runs) and B a [128 (K)][Dn] tile read
 // MN-major.

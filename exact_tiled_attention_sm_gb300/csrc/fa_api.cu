@@ -84,12 +84,12 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
-// fp32 [B*H, N, d] dQ accumulator; boxes of 32 columns x 32 rows x 1 head,
+// fp32 [B*H, N, d] dQ accumulator; boxes of 32 columns x 128 rows x 1 head,
 // 128-byte swizzle; used only as the target of bulk reduce-adds.
 fa_status make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t box[3] = {32, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                         const_cast<void*>(base), dims, strides, box, estr,

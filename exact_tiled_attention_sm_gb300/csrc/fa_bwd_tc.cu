@@ -15,15 +15,16 @@
 // warpgroups (64 query columns each) turn S^T into P^T while the tensor core
 // still computes dP^T, then turn dP^T into scale*dS^T while it already forms
 // dV += P^T dO_i; then dK += dS^T Q_i (P^T and dS^T read straight from TMEM)
-// and dQ_i = dS K (dS read from shared memory).  dQ_i is
-// copied out of TMEM into the just-consumed Q_i / dO_i stage and added into
-// the fp32 dQ accumulator in global memory with TMA bulk reduce-adds, so the
-// tensor memory is free again as soon as it has been read.
+// and dQ_i = dS K (dS read from shared memory).  dQ_i is copied
+// out of TMEM into the just-consumed Q_i / dO_i stage as swizzled fp32 (the
+// tensor memory is free again as soon as it has been read); the load warp,
+// the stage's next user, adds it into the fp32 dQ accumulator in global
+// memory with TMA bulk reduce-adds before reloading the stage.
 //
 // Roles: warps 0-3 dS for query columns 0-63 and the dV epilogue; warps 4-7
-// dS for columns 64-127, the dQ reduction and the dK epilogue; warp 8
+// dS for columns 64-127, the dQ readout and the dK epilogue; warp 8
 // tensor-core issuer and TMEM owner; warp 9 loads (TMA for K, V, Q, dO;
-// plain loads for LSE and D).
+// plain loads for LSE and D) and the dQ bulk reduce-adds.
 //
 // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+d), dK [256+d, 256+2d).
 // P^T overwrites columns [0,32) (queries 0-63) and [64,96) (queries 64-127)
@@ -52,8 +53,8 @@ struct Cfg {
   static constexpr int STAT_BYTES = 2 * 128 * 4;  // LSE*log2(e)[128], D*scale[128]
   static constexpr int OFF_BAR = OFF_STAT + QST * STAT_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
-  static constexpr int B_QFULL = 2, B_QEMPTY = B_QFULL + QST;
-  static constexpr int B_SFULL = B_QEMPTY + QST;   // S^T in TMEM
+  static constexpr int B_QFULL = 2, B_STAGED = B_QFULL + QST;
+  static constexpr int B_SFULL = B_STAGED + QST;   // S^T in TMEM
   static constexpr int B_DPFULL = B_SFULL + 1;      // dP^T in TMEM
   static constexpr int B_PREADY = B_DPFULL + 1;     // P^T written
   static constexpr int B_DSREADY = B_PREADY + 1;    // dS^T written
@@ -89,7 +90,7 @@ struct Params {
 };
 
 enum : uint32_t {
-  SITE_L_KVEMPTY = 1, SITE_L_QEMPTY, SITE_M_KVFULL, SITE_M_QFULL, SITE_M_DQFREE,
+  SITE_L_KVEMPTY = 1, SITE_L_STAGED, SITE_M_KVFULL, SITE_M_QFULL, SITE_M_DQFREE,
   SITE_M_DSREADY, SITE_M_DKDVFREE, SITE_S_QFULL, SITE_S_SFULL, SITE_Q_DQFULL,
   SITE_E_DKDVDONE, SITE_DRAIN, SITE_ALIGN, SITE_M_PREADY, SITE_S_DPFULL
 };
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_KVEMPTY), 1);
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1 + 32);  // TMA arrive + 32 stat writers
-      mbar_init(bar(C::B_QEMPTY + s), 4);      // the 4 dQ-reduction warps
+      mbar_init(bar(C::B_STAGED + s), 128);    // dQ tile staged in the stage
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
@@ -246,15 +247,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------- loads
+    // A Q/dO stage is reused every QST query blocks.  Its previous block's
+    // dQ tile sits in it as fp32 staging (written by the dQ warpgroup): this
+    // warp adds that tile into the accumulator with bulk reduce-adds, waits
+    // until they have read it, then loads the stage's next block.
     if (lane == 0) {
       prefetch_tensormap(&mq);
       prefetch_tensormap(&mk);
       prefetch_tensormap(&mv);
       prefetch_tensormap(&mdo);
+      prefetch_tensormap(&mdq);
     }
     uint32_t qcnt = 0, it = 0;
     int kv_last = -1;
     uint32_t q_used = 0, q_par = 0;
+    int pend_bh[C::QST], pend_q0[C::QST];  // staged dQ tile of each stage
+    for (int s = 0; s < C::QST; ++s) pend_bh[s] = -1, pend_q0[s] = 0;
+    // reduce-adds the dQ tile staged in stage s (lane 0; returns once the
+    // bulk copies have read the staging)
+    auto reduce_out = [&](int s) {
+      if (lane == 0 && pend_bh[s] >= 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint32_t src = c < C::CH ? sQ(s) + c * kChunkBytes
+                                         : sdO(s) + (c - C::CH) * kChunkBytes;
+          tma_reduce_add_3d(&mdq, src, 32 * c, pend_q0[s], pend_bh[s]);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      pend_bh[s] = -1;
+      __syncwarp();
+    };
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
@@ -277,22 +301,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = sc.q_begin(kb); i < sc.n_blk; ++i) {
         const int s = qcnt % C::QST;
         const uint32_t ph = (qcnt / C::QST) & 1;
-        if (!wait_warp(bar(C::B_QEMPTY + s), ph ^ 1, abort_flag, lim,
-                       SITE_L_QEMPTY)) {
-          ok = false;
-          break;
-        }
-        // LSE*log2(e) and D*scale of the block's 128 queries; rows past N
-        // get LSE = +inf so that their P is exactly 0
-        float* st = stat(s);
+        // LSE*log2(e) and D*scale of the block's 128 queries, fetched before
+        // waiting for the stage; rows past N get LSE = +inf so that their P
+        // is exactly 0
         const size_t base = (size_t)bh * N;
+        float lv[4], dv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int qi = lane * 4 + e;
-          const int q = i * 128 + qi;
+          const int q = i * 128 + lane * 4 + e;
           const bool valid = q < N;
-          st[qi] = valid ? p.LSE[base + q] * 1.4426950408889634f : INFINITY;
-          st[128 + qi] = valid ? p.Dvec[base + q] * p.scale : 0.f;
+          lv[e] = valid ? p.LSE[base + q] * 1.4426950408889634f : INFINITY;
+          dv[e] = valid ? p.Dvec[base + q] * p.scale : 0.f;
+        }
+        if (qcnt >= (uint32_t)C::QST) {
+          if (!wait_warp(bar(C::B_STAGED + s), ph ^ 1, abort_flag, lim,
+                         SITE_L_STAGED)) {
+            ok = false;
+            break;
+          }
+          reduce_out(s);
+        }
+        float* st = stat(s);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          st[lane * 4 + e] = lv[e];
+          st[128 + lane * 4 + e] = dv[e];
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES);
@@ -304,13 +337,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mbar_arrive(bar(C::B_QFULL + s));
+        pend_bh[s] = bh;
+        pend_q0[s] = i * 128;
         q_used |= 1u << s;
         q_par = (q_par & ~(1u << s)) | (ph << s);
         ++qcnt;
       }
       ++it;
     }
-    if (lane == 0) {  // every copy issued here lands before the CTA exits
+    // the last QST blocks' dQ tiles (skipped after an abort)
+    if (ok && !*abort_flag) {
+      for (uint32_t k = qcnt > (uint32_t)C::QST ? qcnt - C::QST : 0; k < qcnt; ++k) {
+        const int s = k % C::QST;
+        if (!wait_warp(bar(C::B_STAGED + s), (k / C::QST) & 1, abort_flag, lim,
+                       SITE_L_STAGED))
+          break;
+        reduce_out(s);
+      }
+    }
+    if (lane == 0) {  // every copy issued here completes before the CTA exits
+      bulk_wait_group0();
       volatile int no_abort = 0;
       if (kv_last >= 0)
         wait_one(bar(C::B_KVFULL), (uint32_t)kv_last, &no_abort, lim, SITE_DRAIN);
@@ -336,16 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const int i0 = sc.q_begin(kb);
+        // S^T = K Q_i^T of block qc into TMEM (the previous block's P^T has
+        // been consumed by its dV product, issued earlier by this thread)
+        auto issue_s = [&](uint32_t qc) -> bool {
+          const int st = qc % C::QST;
+          if (!wait_one(bar(C::B_QFULL + st), (qc / C::QST) & 1, abort_flag,
+                        lim, SITE_M_QFULL))
+            return false;
+          tc_fence_after();
+          mma_rows_x_rows<D>(tmem + C::TM_S, sK, sQ(st), C::IDESC_SS);
+          umma_commit(bar(C::B_SFULL));
+          return true;
+        };
+        if (!issue_s(qcnt)) break;
         for (int i = i0; i < sc.n_blk; ++i) {
           const int s = qcnt % C::QST;
-          if (!wait_one(bar(C::B_QFULL + s), (qcnt / C::QST) & 1, abort_flag,
-                        lim, SITE_M_QFULL)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          mma_rows_x_rows<D>(tmem + C::TM_S, sK, sQ(s), C::IDESC_SS);
-          umma_commit(bar(C::B_SFULL));
           if (g > 0) {  // dQ of the previous block has left TMEM
             if (!wait_one(bar(C::B_DQFREE), (g - 1) & 1, abort_flag, lim,
                           SITE_M_DQFREE)) {
@@ -383,6 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                            tmem + C::TM_DP + 64, sQ(s), C::IDESC_TS, !first);
           mma_colsT_x_rows(tmem + C::TM_DP, sDS, sK, C::IDESC_DQ);
           umma_commit(bar(C::B_DQFULL));
+          // the next block's S^T: its Q/dO stage was refilled after the
+          // stage's previous dQ tile had been reduced out, a full block ago
+          if (i + 1 < sc.n_blk && !issue_s(qcnt + 1)) {
+            ok = false;
+            break;
+          }
           ++qcnt;
           ++g;
         }
@@ -466,24 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(bar(C::B_DQFREE));
+          // the staging is read by the load warp's bulk reduce-adds
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int y = q0 + wq * 32;
-            if (y < N) {
-#pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                const uint32_t base = c < C::CH
-                                          ? sQ(s) + c * kChunkBytes
-                                          : sdO(s) + (c - C::CH) * kChunkBytes;
-                tma_reduce_add_3d(&mdq, base + wq * 32 * 128, 32 * c, y, bh);
-              }
-              bulk_commit_group();
-              bulk_wait_group_read0();
-            }
-            mbar_arrive(bar(C::B_QEMPTY + s));
-          }
-          __syncwarp();
+          mbar_arrive(bar(C::B_STAGED + s));
         }
         ++qcnt;
         ++g;
@@ -503,7 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::B_DKDVFREE));
       ++it;
     }
-    if (grp == 1 && lane == 0) bulk_wait_group0();  // reductions complete
   }
 
   tc_fence_before();

@@ -17,6 +17,10 @@ static __device__ unsigned int g_fa_device_status = 0;
 // correct launch makes on the sizes this library accepts.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
+// Suspend-time hint of one polling step of a bounded wait: long next to a
+// pipeline step, short next to the wait's time limit.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 constexpr int kTile = 128;  // rows of a query block and of a key block
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }

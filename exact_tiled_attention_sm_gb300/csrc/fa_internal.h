@@ -15,7 +15,7 @@ struct AttnShape {
 
 // TMA descriptors (built by fa_api.cu): the bf16 [B*H, N, d] tensors with
 // 64-column x 128-row boxes, and the fp32 dQ accumulator [B*H, N, d] with
-// 32-column x 32-row boxes (the backward's bulk reductions); all with the
+// 32-column x 128-row boxes (the backward's bulk reductions); all with the
 // 128-byte swizzle.
 struct TileMaps {
   CUtensorMap q, k, v, o, dO, dq_acc;

@@ -67,6 +67,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but lets the hardware suspend the thread until the phase
+// completes or about `hint_ns` nanoseconds pass, so a waiting warp does not
+// take issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar,
+                                                    uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Records a timeout once per launch (first writer wins) and raises the CTA's
 // abort flag.
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag,
@@ -83,7 +100,7 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity,
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       record_timeout(abort_flag, site);

@@ -17,29 +17,48 @@ namespace fa {
 
 constexpr int kChunkBytes = 128 * 128;  // one 64-column chunk of 128 rows
 
+// Shared-memory descriptors of a tile (see sdesc_sw128) read K-major and
+// MN-major.  The start-address field is the descriptor's low bits (address
+// >> 4), so moving a descriptor by `bytes` within shared memory is adding
+// bytes >> 4: the MMA sequences below build one descriptor per tile and step
+// it with adds, which keeps the single issuing thread's cost per MMA small.
+__device__ __forceinline__ uint64_t kdesc(uint32_t saddr) {
+  return sdesc_sw128(saddr, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mdesc(uint32_t saddr) {
+  return sdesc_sw128(saddr, kChunkBytes, 1024);
+}
+// K-major step kk (16 elements): 32 bytes inside a 128-byte row, a new
+// 64-column chunk every 4 steps.
+__host__ __device__ constexpr uint32_t kstep(int kk) {
+  return (uint32_t)(((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4);
+}
+// MN-major step kk (16 rows of 128 bytes).
+__host__ __device__ constexpr uint32_t mstep(int kk) {
+  return (uint32_t)((kk * 16 * 128) >> 4);
+}
+
 // D(128 x 128) (+)= A B^T with A, B both [128][Dk] K-major tiles (Dk/16 MMAs
-// of K = 16; the 16-element step moves 32 bytes inside a 128-byte row).
+// of K = 16).
 template <int Dk>
 __device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t sa,
                                                 uint32_t sb, uint32_t idesc) {
+  const uint64_t da = kdesc(sa), db = kdesc(sb);
 #pragma unroll
-  for (int kk = 0; kk < Dk / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-    umma_ss(d_tmem, sdesc_sw128(sa + off, 16, 1024),
-            sdesc_sw128(sb + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-  }
+  for (int kk = 0; kk < Dk / 16; ++kk)
+    umma_ss(d_tmem, da + kstep(kk), db + kstep(kk), idesc, kk > 0 ? 1u : 0u);
 }
 
 // D(128 x Dn) (+)= A B with A (128 x 128) in TMEM (bf16 pairs, lanes = rows)
-// and B a [128][Dn] tile read MN-major (8 MMAs of K = 16 rows; a step moves
-// 16 rows = 2048 bytes; the Dn/64 chunks are kChunkBytes apart).
+// and B a [128][Dn] tile read MN-major (8 MMAs of K = 16 rows; the Dn/64
+// chunks are kChunkBytes apart).
 __device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem,
                                                 uint32_t sb, uint32_t idesc,
                                                 bool accumulate) {
+  const uint64_t db = mdesc(sb);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    umma_ts(d_tmem, a_tmem + kk * 8,
-            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
+    umma_ts(d_tmem, a_tmem + kk * 8, db + mstep(kk), idesc,
             (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -49,11 +68,11 @@ __device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem
 __device__ __forceinline__ void mma_tmem2_x_rows(uint32_t d_tmem, uint32_t a_lo,
                                                  uint32_t a_hi, uint32_t sb,
                                                  uint32_t idesc, bool accumulate) {
+  const uint64_t db = mdesc(sb);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     umma_ts(d_tmem, kk < 4 ? a_lo + kk * 8 : a_hi + (kk - 4) * 8,
-            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
-            (accumulate || kk > 0) ? 1u : 0u);
+            db + mstep(kk), idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // D(128 x Dn) = A B with A^T a [128 (K)][128 (M)] tile read MN-major (its
@@ -61,11 +80,10 @@ __device__ __forceinline__ void mma_tmem2_x_rows(uint32_t d_tmem, uint32_t a_lo,
 // MN-major.
 __device__ __forceinline__ void mma_colsT_x_rows(uint32_t d_tmem, uint32_t sat,
                                                  uint32_t sb, uint32_t idesc) {
+  const uint64_t da = mdesc(sat), db = mdesc(sb);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    umma_ss(d_tmem, sdesc_sw128(sat + kk * 16 * 128, kChunkBytes, 1024),
-            sdesc_sw128(sb + kk * 16 * 128, kChunkBytes, 1024), idesc,
-            kk > 0 ? 1u : 0u);
+    umma_ss(d_tmem, da + mstep(kk), db + mstep(kk), idesc, kk > 0 ? 1u : 0u);
 }
 
 // Byte offset of the 16-byte piece `p` (0..15 across a 128-element row) of

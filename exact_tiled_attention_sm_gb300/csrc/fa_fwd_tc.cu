@@ -333,7 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q >= sc.n_q_tiles) continue;
       const int nt = sc.n_kv(q);
       const int row = q * 128 + wq * 32 + lane;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY;     // running row maximum of the raw scores
+      float mref = -INFINITY;  // exponent reference of l and O_t (log2 units)
+      float l = 0.f;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         if (!wait_warp(bar(C::B_SFULL + t), scnt & 1, abort_flag, lim,
@@ -353,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence32(r1);
         reg_fence32(r2);
         reg_fence32(r3);
-        float x[128];
+        float x[128];  // raw scores q.k of this row
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(r0[i]) * sl2;
-          x[32 + i] = __uint_as_float(r1[i]) * sl2;
-          x[64 + i] = __uint_as_float(r2[i]) * sl2;
-          x[96 + i] = __uint_as_float(r3[i]) * sl2;
+          x[i] = __uint_as_float(r0[i]);
+          x[32 + i] = __uint_as_float(r1[i]);
+          x[64 + i] = __uint_as_float(r2[i]);
+          x[96 + i] = __uint_as_float(r3[i]);
         }
         if (sc.needs_mask(q, j)) {
           const int k0 = j * 128;
@@ -368,44 +370,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (k0 + i >= lim_k) x[i] = -INFINITY;
         }
-        float tmax = x[0];
+        // Row maximum of the raw scores (scale > 0 commutes with max): eight
+        // independent chains of three-input maxima, then a short tree.
+        float mk[8];
 #pragma unroll
-        for (int i = 1; i < 128; ++i) tmax = fmaxf(tmax, x[i]);
-        const float m_new = fmaxf(m, tmax);
-        // a row with nothing visible yet keeps 0 as its reference
-        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2_approx(m - m_ref);  // m = -inf -> 0
-        float rs = 0.f;
+        for (int k = 0; k < 8; ++k) mk[k] = fmax3(x[k], x[8 + k], x[16 + k]);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          x[i] = ex2_approx(x[i] - m_ref);
-          rs += x[i];
+        for (int i = 24; i < 120; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[i + k], x[i + 8 + k]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], x[120 + k]);
+        m = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
+                  fmax3(mk[6], mk[7], m));
+        // exponent reference in log2 units; a row with nothing visible yet
+        // keeps 0 as its reference
+        const float mref_new = (m == -INFINITY) ? 0.f : m * sl2;
+        const float alpha = ex2_approx(mref - mref_new);  // no reference yet -> 0
+        mref = mref_new;
+        // P = 2^(scale*log2(e)*s - mref): one packed fma per pair, row sum
+        // in four packed accumulators
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-mref_new, -mref_new);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = 32 * h + 2 * i;
+            float a, b;
+            f2_unpack(ffma2(f2_pack(x[e], x[e + 1]), sl2x2, nm2), a, b);
+            a = ex2_approx(a);
+            b = ex2_approx(b);
+            acc[i & 3] = fadd2(acc[i & 3], f2_pack(a, b));
+            pk[i] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tS + 16 * h, pk);
         }
-        l = l * alpha + rs;
-        m = m_new;
-        {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-          tmem_st32(tS + 0, pk);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            pk[i] = pack_bf16x2(x[64 + 2 * i], x[64 + 2 * i + 1]);
-          tmem_st32(tS + 32, pk);
-        }
+        float rs_lo, rs_hi;
+        f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), rs_lo, rs_hi);
+        l = l * alpha + (rs_lo + rs_hi);
         // O_t *= alpha when this warp's rows moved their max (the previous
-        // P V product into O_t completed before S_t of this block did)
+        // P V product into O_t completed before S_t of this block did): all
+        // column chunks loaded under one wait, scaled in pairs, stored back
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t o[D / 32][32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o[c]);
+          tmem_ld_wait();
+          const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_ld_wait();
-            reg_fence32(o);
+            reg_fence32(o[c]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + 32 * c, o);
+            for (int i = 0; i < 16; ++i) {
+              float a, b;
+              f2_unpack(fmul2(f2_pack(__uint_as_float(o[c][2 * i]),
+                                      __uint_as_float(o[c][2 * i + 1])),
+                              al2),
+                        a, b);
+              o[c][2 * i] = __float_as_uint(a);
+              o[c][2 * i + 1] = __float_as_uint(b);
+            }
+            tmem_st32(tO + 32 * c, o[c]);
           }
         }
         tmem_st_wait();
@@ -440,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (store)
-        p.LSE[(size_t)bh * sc.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+        p.LSE[(size_t)bh * sc.N + row] = (mref + log2f(l)) * 0.69314718055994531f;
       // all TMEM reads of O_t are done before the next item's first P V
       // product (ordered by this group's next p_ready arrival)
       tc_fence_before();

@@ -50,10 +50,12 @@ struct Cfg {
   static constexpr int OFF_DO = OFF_Q + QST * TILE_BYTES;
   static constexpr int OFF_DS = OFF_DO + QST * TILE_BYTES;   // dS^T [128][128]
   static constexpr int OFF_STAT = OFF_DS + 2 * kChunkBytes;  // per stage
-  static constexpr int STAT_BYTES = 2 * 128 * 4;  // LSE*log2(e)[128], D*scale[128]
+  static constexpr int STAT_BYTES = 2 * 128 * 4;  // -LSE*log2(e)[128], -D*scale[128]
   static constexpr int OFF_BAR = OFF_STAT + QST * STAT_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1;
-  static constexpr int B_QFULL = 2, B_STAGED = B_QFULL + QST;
+  static constexpr int B_QFULL = 2;                 // Q_i and the stats
+  static constexpr int B_DOFULL = B_QFULL + QST;    // dO_i
+  static constexpr int B_STAGED = B_DOFULL + QST;
   static constexpr int B_SFULL = B_STAGED + QST;   // S^T in TMEM
   static constexpr int B_DPFULL = B_SFULL + 1;      // dP^T in TMEM
   static constexpr int B_PREADY = B_DPFULL + 1;     // P^T written
@@ -92,72 +94,99 @@ struct Params {
 enum : uint32_t {
   SITE_L_KVEMPTY = 1, SITE_L_STAGED, SITE_M_KVFULL, SITE_M_QFULL, SITE_M_DQFREE,
   SITE_M_DSREADY, SITE_M_DKDVFREE, SITE_S_QFULL, SITE_S_SFULL, SITE_Q_DQFULL,
-  SITE_E_DKDVDONE, SITE_DRAIN, SITE_ALIGN, SITE_M_PREADY, SITE_S_DPFULL
+  SITE_E_DKDVDONE, SITE_DRAIN, SITE_ALIGN, SITE_M_PREADY, SITE_S_DPFULL,
+  SITE_M_DOFULL
 };
 
 // One warpgroup's half of the softmax-gradient step for query block i:
 // chunks c0, c0+1 of 32 query columns; thread = key row r (TMEM lane).
 // Phase P (needs only S^T): P^T = 2^(S*scale*log2(e) - LSE*log2(e)), kept in
 // fp32 registers and written to TMEM as bf16 at `pcol` (columns relative to
-// the S^T block, inside the columns this warpgroup has read).
+// the S^T block, inside the columns this warpgroup has read).  `nlse2` holds
+// -LSE*log2(e) per query (-inf past N, so those columns are exactly 0).
 __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
-                                       const float* lse2, int c0, uint32_t pcol,
+                                       const float* nlse2, int c0, uint32_t pcol,
                                        int key, bool kvalid, bool diag, int q0,
                                        float sl2, float (&pr)[64]) {
+  uint32_t sr[2][32];
+  tmem_ld32(tmem_row + tm_s + 32 * c0, sr[0]);
+  tmem_ld32(tmem_row + tm_s + 32 * (c0 + 1), sr[1]);
+  tmem_ld_wait();
+  reg_fence32(sr[0]);
+  reg_fence32(sr[1]);
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(nlse2 + 32 * c0);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int c = c0 + h;
-    uint32_t sr[32];
-    tmem_ld32(tmem_row + tm_s + 32 * c, sr);
-    tmem_ld_wait();
-    reg_fence32(sr);
-    const float4* l4 = reinterpret_cast<const float4*>(lse2 + 32 * c);
-    uint32_t pp[16];
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const float4 lv = l4[e / 4];
-      const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+      const ulonglong2 lv = l4[(32 * h + e) / 4];
+      float* o = pr + 32 * h + e;
+      f2_unpack(ffma2(f2_pack(__uint_as_float(sr[h][e]), __uint_as_float(sr[h][e + 1])),
+                      sl2x2, lv.x),
+                o[0], o[1]);
+      f2_unpack(ffma2(f2_pack(__uint_as_float(sr[h][e + 2]), __uint_as_float(sr[h][e + 3])),
+                      sl2x2, lv.y),
+                o[2], o[3]);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float v = ex2_approx(fmaf(__uint_as_float(sr[e + u]), sl2, -la[u]));
-        if (diag && q0 + 32 * c + e + u < key) v = 0.f;
-        if (!kvalid) v = 0.f;
-        pr[32 * h + e + u] = v;
-      }
-      pp[e / 2] = pack_bf16x2(pr[32 * h + e], pr[32 * h + e + 1]);
-      pp[e / 2 + 1] = pack_bf16x2(pr[32 * h + e + 2], pr[32 * h + e + 3]);
+      for (int u = 0; u < 4; ++u) o[u] = ex2_approx(o[u]);
     }
+  // causal diagonal block: keys after the query are invisible; key rows past
+  // N (ragged last block) are zeroed too (both warp-uniform, rare branches)
+  if (diag) {
+#pragma unroll
+    for (int x = 0; x < 64; ++x)
+      if (q0 + 32 * c0 + x < key) pr[x] = 0.f;
+  }
+  if (__any_sync(0xffffffffu, !kvalid)) {
+#pragma unroll
+    for (int x = 0; x < 64; ++x) pr[x] = kvalid ? pr[x] : 0.f;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pp[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) pp[k] = pack_bf16x2(pr[32 * h + 2 * k], pr[32 * h + 2 * k + 1]);
     tmem_st16(tmem_row + tm_s + pcol + 16 * h, pp);
   }
 }
 
 // Phase dS (needs dP^T): scale*dS^T = P * (dP*scale - D*scale), written to
-// TMEM at `pcol` of the dP^T block and to the swizzled shared tile.
+// TMEM at `pcol` of the dP^T block and to the swizzled shared tile.  `ndsc`
+// holds -D*scale per query.
 template <int D>
 __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
-                                        const float* dsc, int c0, uint32_t pcol,
+                                        const float* ndsc, int c0, uint32_t pcol,
                                         int r, float scale,
                                         const float (&pr)[64]) {
   using C = Cfg<D>;
+  uint32_t dr[2][32];
+  tmem_ld32(tmem_row + C::TM_DP + 32 * c0, dr[0]);
+  tmem_ld32(tmem_row + C::TM_DP + 32 * (c0 + 1), dr[1]);
+  tmem_ld_wait();
+  reg_fence32(dr[0]);
+  reg_fence32(dr[1]);
+  const uint64_t sc2 = f2_pack(scale, scale);
+  const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(ndsc + 32 * c0);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int c = c0 + h;
-    uint32_t dr[32];
-    tmem_ld32(tmem_row + C::TM_DP + 32 * c, dr);
-    tmem_ld_wait();
-    reg_fence32(dr);
-    const float4* d4 = reinterpret_cast<const float4*>(dsc + 32 * c);
     uint32_t dd[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
-      const float4 dv = d4[e / 4];
-      const float da[4] = {dv.x, dv.y, dv.z, dv.w};
-      float ds[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        ds[u] = pr[32 * h + e + u] * fmaf(__uint_as_float(dr[e + u]), scale, -da[u]);
-      dd[e / 2] = pack_bf16x2(ds[0], ds[1]);
-      dd[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+      const ulonglong2 dv = d4[(32 * h + e) / 4];
+      const float* pe = pr + 32 * h + e;
+      float a0, a1, a2, a3;
+      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(dr[h][e]), __uint_as_float(dr[h][e + 1])),
+                            sc2, dv.x),
+                      f2_pack(pe[0], pe[1])),
+                a0, a1);
+      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(dr[h][e + 2]), __uint_as_float(dr[h][e + 3])),
+                            sc2, dv.y),
+                      f2_pack(pe[2], pe[3])),
+                a2, a3);
+      dd[e / 2] = pack_bf16x2(a0, a1);
+      dd[e / 2 + 1] = pack_bf16x2(a2, a3);
     }
     tmem_st16(tmem_row + C::TM_DP + pcol + 16 * h, dd);
 #pragma unroll
@@ -220,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_KVEMPTY), 1);
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1 + 32);  // TMA arrive + 32 stat writers
+      mbar_init(bar(C::B_DOFULL + s), 1);
       mbar_init(bar(C::B_STAGED + s), 128);    // dQ tile staged in the stage
     }
     mbar_init(bar(C::B_SFULL), 1);
@@ -263,20 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t q_used = 0, q_par = 0;
     int pend_bh[C::QST], pend_q0[C::QST];  // staged dQ tile of each stage
     for (int s = 0; s < C::QST; ++s) pend_bh[s] = -1, pend_q0[s] = 0;
-    // reduce-adds the dQ tile staged in stage s (lane 0; returns once the
-    // bulk copies have read the staging)
-    auto reduce_out = [&](int s) {
+    // reduce-adds one half of the dQ tile staged in stage s: half 0 is the
+    // part held in the Q buffer (columns [0, d/2)), half 1 the part in the dO
+    // buffer.  Lane 0; returns once the bulk copies have read that buffer.
+    auto reduce_half = [&](int s, int half) {
       if (lane == 0 && pend_bh[s] >= 0) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint32_t src = c < C::CH ? sQ(s) + c * kChunkBytes
-                                         : sdO(s) + (c - C::CH) * kChunkBytes;
-          tma_reduce_add_3d(&mdq, src, 32 * c, pend_q0[s], pend_bh[s]);
+        for (int c = 0; c < C::CH; ++c) {  // 32-column fp32 boxes
+          const uint32_t src = (half ? sdO(s) : sQ(s)) + c * kChunkBytes;
+          tma_reduce_add_3d(&mdq, src, 32 * (c + C::CH * half), pend_q0[s],
+                            pend_bh[s]);
         }
         bulk_commit_group();
         bulk_wait_group_read0();
       }
-      pend_bh[s] = -1;
       __syncwarp();
     };
     bool ok = true;
@@ -310,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int q = i * 128 + lane * 4 + e;
           const bool valid = q < N;
-          lv[e] = valid ? p.LSE[base + q] * 1.4426950408889634f : INFINITY;
-          dv[e] = valid ? p.Dvec[base + q] * p.scale : 0.f;
+          lv[e] = valid ? -p.LSE[base + q] * 1.4426950408889634f : -INFINITY;
+          dv[e] = valid ? -p.Dvec[base + q] * p.scale : 0.f;
         }
         if (qcnt >= (uint32_t)C::QST) {
           if (!wait_warp(bar(C::B_STAGED + s), ph ^ 1, abort_flag, lim,
@@ -319,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          reduce_out(s);
+          reduce_half(s, 0);
         }
         float* st = stat(s);
 #pragma unroll
@@ -327,16 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           st[lane * 4 + e] = lv[e];
           st[128 + lane * 4 + e] = dv[e];
         }
+        // Q_i first: S^T and the P phase need only Q_i and the stats
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES);
-          for (int c = 0; c < C::CH; ++c) {
+          mbar_arrive_expect_tx(bar(C::B_QFULL + s), C::TILE_BYTES);
+          for (int c = 0; c < C::CH; ++c)
             tma_load_3d(sQ(s) + c * kChunkBytes, &mq, bar(C::B_QFULL + s),
                         c * 64, i * 128, bh);
-            tma_load_3d(sdO(s) + c * kChunkBytes, &mdo, bar(C::B_QFULL + s),
-                        c * 64, i * 128, bh);
-          }
         }
         mbar_arrive(bar(C::B_QFULL + s));
+        if (qcnt >= (uint32_t)C::QST) reduce_half(s, 1);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::B_DOFULL + s), C::TILE_BYTES);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(sdO(s) + c * kChunkBytes, &mdo, bar(C::B_DOFULL + s),
+                        c * 64, i * 128, bh);
+        }
         pend_bh[s] = bh;
         pend_q0[s] = i * 128;
         q_used |= 1u << s;
@@ -352,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(bar(C::B_STAGED + s), (k / C::QST) & 1, abort_flag, lim,
                        SITE_L_STAGED))
           break;
-        reduce_out(s);
+        reduce_half(s, 0);
+        reduce_half(s, 1);
       }
     }
     if (lane == 0) {  // every copy issued here completes before the CTA exits
@@ -361,9 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kv_last >= 0)
         wait_one(bar(C::B_KVFULL), (uint32_t)kv_last, &no_abort, lim, SITE_DRAIN);
       for (int s = 0; s < C::QST; ++s)
-        if ((q_used >> s) & 1)
+        if ((q_used >> s) & 1) {
           wait_one(bar(C::B_QFULL + s), (q_par >> s) & 1, &no_abort, lim,
                    SITE_DRAIN);
+          wait_one(bar(C::B_DOFULL + s), (q_par >> s) & 1, &no_abort, lim,
+                   SITE_DRAIN);
+        }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -405,6 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
           }
+          if (!wait_one(bar(C::B_DOFULL + s), (qcnt / C::QST) & 1, abort_flag,
+                        lim, SITE_M_DOFULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           mma_rows_x_rows<D>(tmem + C::TM_DP, sV, sdO(s), C::IDESC_SS);
           umma_commit(bar(C::B_DPFULL));
           if (!wait_one(bar(C::B_PREADY), g & 1, abort_flag, lim,

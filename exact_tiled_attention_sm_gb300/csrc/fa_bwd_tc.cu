@@ -14,17 +14,21 @@
 // transposed tiles S^T = K Q_i^T and dP^T = V dO_i^T (rows = keys); two
 // warpgroups (64 query columns each) turn S^T into P^T while the tensor core
 // still computes dP^T, then turn dP^T into scale*dS^T while it already forms
-// dV += P^T dO_i; then dK += dS^T Q_i (P^T and dS^T read straight from TMEM)
-// and dQ_i = dS K (dS read from shared memory).  dQ_i is copied
-// out of TMEM into the just-consumed Q_i / dO_i stage as swizzled fp32 (the
-// tensor memory is free again as soon as it has been read); the load warp,
-// the stage's next user, adds it into the fp32 dQ accumulator in global
-// memory with TMA bulk reduce-adds before reloading the stage.
+// dV += P^T dO_i; then dK += dS^T Q_i (P^T and dS^T read straight from TMEM,
+// so these two products read only one operand from shared memory) and
+// dQ_i = dS K (dS read from shared memory).  Shared-memory reads by anything
+// other than the tensor core make progress mostly while it runs such
+// TMEM-operand products.  dQ_i is copied out of TMEM by both warpgroups into the
+// just-consumed Q_i / dO_i stage as swizzled fp32 (the tensor memory is
+// released as soon as it has been read); the load warp, the stage's next
+// user, adds it into the fp32 dQ accumulator in global memory with TMA bulk
+// reduce-adds before reloading the stage, Q_i first.
 //
-// Roles: warps 0-3 dS for query columns 0-63 and the dV epilogue; warps 4-7
-// dS for columns 64-127, the dQ readout and the dK epilogue; warp 8
-// tensor-core issuer and TMEM owner; warp 9 loads (TMA for K, V, Q, dO;
-// plain loads for LSE and D) and the dQ bulk reduce-adds.
+// Roles: warps 0-3 dS for query columns 0-63, half of the dQ readout and the
+// dV epilogue; warps 4-7 dS for columns 64-127, the other half of the dQ
+// readout and the dK epilogue; warp 8 tensor-core issuer and TMEM owner;
+// warp 9 loads (TMA for K, V, Q, dO; plain loads for LSE and D) and the dQ
+// bulk reduce-adds.
 //
 // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+d), dK [256+d, 256+2d).
 // P^T overwrites columns [0,32) (queries 0-63) and [64,96) (queries 64-127)
@@ -151,9 +155,10 @@ __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
   }
 }
 
-// Phase dS (needs dP^T): scale*dS^T = P * (dP*scale - D*scale), written to
-// TMEM at `pcol` of the dP^T block and to the swizzled shared tile.  `ndsc`
-// holds -D*scale per query.
+// Phase dS (needs dP^T): scale*dS^T = P * (dP*scale - D*scale), written as
+// bf16 to TMEM at `pcol` of the dP^T block (the dK product's A operand) and
+// to the swizzled shared tile (row = key r; the dQ product's A operand).
+// `ndsc` holds -D*scale per query.
 template <int D>
 __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
                                         const float* ndsc, int c0, uint32_t pcol,
@@ -250,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::QST; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1 + 32);  // TMA arrive + 32 stat writers
       mbar_init(bar(C::B_DOFULL + s), 1);
-      mbar_init(bar(C::B_STAGED + s), 128);    // dQ tile staged in the stage
+      mbar_init(bar(C::B_STAGED + s), 256);    // dQ tile staged in the stage
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PREADY), 256);
     mbar_init(bar(C::B_DSREADY), 256);
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQFREE), 128);
+    mbar_init(bar(C::B_DQFREE), 256);
     mbar_init(bar(C::B_DKDVDONE), 1);
     mbar_init(bar(C::B_DKDVFREE), 256);
     mbar_init(bar(C::B_MMADONE), 1);
@@ -309,12 +314,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    // LSE and D of a block's 128 queries (4 per lane), loaded one block
+    // ahead so that their latency is hidden behind a whole block of work:
+    // raw values from clamped addresses, validity applied when they are
+    // written to the stage
+    float lraw[4] = {0.f, 0.f, 0.f, 0.f}, draw[4] = {0.f, 0.f, 0.f, 0.f};
+    auto fetch_stats = [&](int bh_, int i_) {
+      const size_t base = (size_t)bh_ * N;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q = min(i_ * 128 + lane * 4 + e, N - 1);
+        lraw[e] = p.LSE[base + q];
+        draw[e] = p.Dvec[base + q];
+      }
+    };
+    // the first block this CTA processes
+    for (int w = 0; w < nw; ++w) {
+      const int item = sc.item_of(blockIdx.x, w);
+      if (item < 0) continue;
+      int bh0, kb0;
+      sc.decode(item, bh0, kb0);
+      fetch_stats(bh0, sc.q_begin(kb0));
+      break;
+    }
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
       if (item < 0) continue;
       int bh, kb;
       sc.decode(item, bh, kb);
+      // the block after this item's last one: the next item's first block
+      int nbh = -1, ni = 0;
+      for (int w2 = w + 1; w2 < nw; ++w2) {
+        const int item2 = sc.item_of(blockIdx.x, w2);
+        if (item2 < 0) continue;
+        int kb2;
+        sc.decode(item2, nbh, kb2);
+        ni = sc.q_begin(kb2);
+        break;
+      }
       if (it > 0 && !wait_warp(bar(C::B_KVEMPTY), (it - 1) & 1, abort_flag, lim,
                                SITE_L_KVEMPTY))
         break;
@@ -331,18 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = sc.q_begin(kb); i < sc.n_blk; ++i) {
         const int s = qcnt % C::QST;
         const uint32_t ph = (qcnt / C::QST) & 1;
-        // LSE*log2(e) and D*scale of the block's 128 queries, fetched before
-        // waiting for the stage; rows past N get LSE = +inf so that their P
-        // is exactly 0
-        const size_t base = (size_t)bh * N;
+        // -LSE*log2(e) and -D*scale of this block's queries (fetched during
+        // the previous block); rows past N get -inf so that their P is
+        // exactly 0.  Then the next block's values are requested.
         float lv[4], dv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int q = i * 128 + lane * 4 + e;
-          const bool valid = q < N;
-          lv[e] = valid ? -p.LSE[base + q] * 1.4426950408889634f : -INFINITY;
-          dv[e] = valid ? -p.Dvec[base + q] * p.scale : 0.f;
+          const bool valid = i * 128 + lane * 4 + e < N;
+          lv[e] = valid ? -lraw[e] * 1.4426950408889634f : -INFINITY;
+          dv[e] = valid ? -draw[e] * p.scale : 0.f;
         }
+        if (i + 1 < sc.n_blk)
+          fetch_stats(bh, i + 1);
+        else if (nbh >= 0)
+          fetch_stats(nbh, ni);
         if (qcnt >= (uint32_t)C::QST) {
           if (!wait_warp(bar(C::B_STAGED + s), ph ^ 1, abort_flag, lim,
                          SITE_L_STAGED)) {
@@ -543,32 +583,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(C::B_DSREADY));
-        if (grp == 1) {
-          // dQ_i: TMEM -> swizzled fp32 staging in the consumed Q/dO stage ->
-          // bulk reduce-add into the accumulator, 32 rows per warp
-          if (!wait_warp(bar(C::B_DQFULL), g & 1, abort_flag, lim,
-                         SITE_Q_DQFULL)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        // dQ_i, both warpgroups, d/2 columns each: TMEM -> registers (the
+        // columns are released at once for the next dP^T) -> swizzled fp32
+        // staging in the consumed stage (group 0 in the Q buffer, group 1 in
+        // the dO buffer), which the load warp bulk reduce-adds into the
+        // accumulator before refilling the stage
+        if (!wait_warp(bar(C::B_DQFULL), g & 1, abort_flag, lim, SITE_Q_DQFULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
+          constexpr int NC = D / 64;  // 32-column chunks per group
+          uint32_t v[NC][32];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem_row + C::TM_DP + 32 * c, v);
-            tmem_ld_wait();
-            reg_fence32(v);
-            const uint32_t base =
-                c < C::CH ? sQ(s) + c * kChunkBytes : sdO(s) + (c - C::CH) * kChunkBytes;
-            uint8_t* row = smem + (base - sb) + r * 128;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4*>(row + ((k ^ (r & 7)) << 4)) =
-                  make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-          }
+          for (int c = 0; c < NC; ++c)
+            tmem_ld32(tmem_row + C::TM_DP + 32 * (NC * grp + c), v[c]);
+          tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(bar(C::B_DQFREE));
-          // the staging is read by the load warp's bulk reduce-adds
+          uint8_t* stg = smem + ((grp ? sdO(s) : sQ(s)) - sb) + r * 128;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            reg_fence32(v[c]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<uint4*>(stg + c * kChunkBytes + ((k ^ (r & 7)) << 4)) =
+                  make_uint4(v[c][4 * k], v[c][4 * k + 1], v[c][4 * k + 2], v[c][4 * k + 3]);
+          }
           fence_proxy_async_smem();
           mbar_arrive(bar(C::B_STAGED + s));
         }

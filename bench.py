@@ -51,17 +51,29 @@ def measured_peaks():
         return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def profile_traffic(kernel_key):
-    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if the
-    summary was taken on the current kernel sources; else None."""
+# kernel key (as in profiles/traffic.txt) -> the source file that defines it
+KERNEL_SOURCES = {"bwd_kernel": "fa_bwd_tc.cu", "fwd_kernel": "fa_fwd_tc.cu"}
+
+
+def kernel_digest(kernel_key):
+    """sha256 (first 16 hex digits) of the kernel's .cu file and every shared
+    header of csrc/: the sources a capture of that kernel depends on."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "exact_tiled_attention_sm_gb300", "csrc")
+    cu = next(v for k, v in KERNEL_SOURCES.items() if kernel_key.startswith(k))
+    files = [cu] + sorted(f for f in os.listdir(src) if f.endswith((".cuh", ".h")))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(src)):
+    for f in files:
         with open(os.path.join(src, f), "rb") as fh:
             h.update(fh.read())
-    digest = h.hexdigest()[:16]
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary, if the
+    summary was taken on the kernel's current sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    digest = kernel_digest(kernel_key)
     try:
         for line in open(path):
             parts = line.split()

@@ -353,6 +353,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ni = sc.q_begin(kb2);
         break;
       }
+      // The stage this item's first block will use still holds the staged
+      // dQ of an earlier block: add it out now, while the previous item's
+      // last blocks are still being computed, instead of after the K/V swap.
+      if (qcnt >= (uint32_t)C::QST) {
+        const int s = qcnt % C::QST;
+        if (!wait_warp(bar(C::B_STAGED + s), ((qcnt / C::QST) & 1) ^ 1, abort_flag,
+                       lim, SITE_L_STAGED))
+          break;
+        reduce_half(s, 0);
+        reduce_half(s, 1);
+        pend_bh[s] = -1;
+      }
       if (it > 0 && !wait_warp(bar(C::B_KVEMPTY), (it - 1) & 1, abort_flag, lim,
                                SITE_L_KVEMPTY))
         break;

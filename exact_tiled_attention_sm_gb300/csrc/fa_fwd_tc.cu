@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           umma_commit(bar(C::B_KEMPTY + s));
           ++kcnt;
+          // the Q tiles are read by S products only: with a single key block
+          // they are free for the next item as soon as these complete
+          if (n_kv == 1) umma_commit(bar(C::B_QEMPTY));
         }
         for (int j = 0; j < n_kv && ok; ++j) {
           const int vs = vcnt % C::VST;
@@ -303,9 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(bar(C::B_KEMPTY + ks));
             ++kcnt;
           }
+          // the item's last S products have been issued: the next item's Q
+          // tiles may load while its last P V products and epilogue run
+          if (ok && j + 2 == n_kv) umma_commit(bar(C::B_QEMPTY));
         }
         if (!ok) break;
-        umma_commit(bar(C::B_QEMPTY));
         ++it;
       }
       // every MMA issued by this thread completes before TMEM is released

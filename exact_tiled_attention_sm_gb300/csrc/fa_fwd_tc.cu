@@ -397,9 +397,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // in four packed accumulators
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t nm2 = f2_pack(-mref_new, -mref_new);
+        // O_t *= alpha is needed when a row of this warp moved its max (the
+        // previous P V product into O_t completed before S_t of this block
+        // did).  O's first 64 columns are requested (always, which keeps the
+        // register allocation free of branches) before the last quarter of
+        // the exponentials, so that their TMEM latency hides behind it.
+        const bool resc = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+        uint32_t oa[2][32];
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
+          if (h == 3) {
+            tmem_ld32(tO + 0, oa[0]);
+            tmem_ld32(tO + 32, oa[1]);
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -416,29 +427,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rs_lo, rs_hi;
         f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), rs_lo, rs_hi);
         l = l * alpha + (rs_lo + rs_hi);
-        // O_t *= alpha when this warp's rows moved their max (the previous
-        // P V product into O_t completed before S_t of this block did): all
-        // column chunks loaded under one wait, scaled in pairs, stored back
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t o[D / 32][32];
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o[c]);
-          tmem_ld_wait();
+        // the loaded registers stay untouched until the load has landed
+        tmem_ld_wait();
+        reg_fence32(oa[0]);
+        reg_fence32(oa[1]);
+        if (resc) {
           const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            reg_fence32(o[c]);
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               float a, b;
-              f2_unpack(fmul2(f2_pack(__uint_as_float(o[c][2 * i]),
-                                      __uint_as_float(o[c][2 * i + 1])),
+              f2_unpack(fmul2(f2_pack(__uint_as_float(oa[c][2 * i]),
+                                      __uint_as_float(oa[c][2 * i + 1])),
                               al2),
                         a, b);
-              o[c][2 * i] = __float_as_uint(a);
-              o[c][2 * i + 1] = __float_as_uint(b);
+              oa[c][2 * i] = __float_as_uint(a);
+              oa[c][2 * i + 1] = __float_as_uint(b);
             }
-            tmem_st32(tO + 32 * c, o[c]);
+            tmem_st32(tO + 32 * c, oa[c]);
+          }
+#pragma unroll
+          for (int c = 2; c < D / 32; ++c) {  // the remaining columns
+            uint32_t ob[32];
+            tmem_ld32(tO + 32 * c, ob);
+            tmem_ld_wait();
+            reg_fence32(ob);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a, b;
+              f2_unpack(fmul2(f2_pack(__uint_as_float(ob[2 * i]),
+                                      __uint_as_float(ob[2 * i + 1])),
+                              al2),
+                        a, b);
+              ob[2 * i] = __float_as_uint(a);
+              ob[2 * i + 1] = __float_as_uint(b);
+            }
+            tmem_st32(tO + 32 * c, ob);
           }
         }
         tmem_st_wait();

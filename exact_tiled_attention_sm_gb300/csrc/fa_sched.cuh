@@ -22,9 +22,16 @@ namespace fa {
 // Under the causal mask a head group holds about this many waves of items:
 // enough for the snake order to pair heavy with light items within the
 // group, few enough heads that the group's K/V (forward) or Q/dO (backward)
-// stay resident in L2.  Without the mask every item costs the same and one
-// wave per group keeps the most reuse.
-constexpr int kGroupWaves = 4;
+// mostly stay in L2.  Eight waves balance the per-CTA work to within 2-3% on
+// the measured shapes (N = 2048 ... 32768), where four left the last,
+// partial group's heaviest items in one wave (a 21% loss at N = 16384).
+// Without the mask every item costs the same and one wave per group keeps the
+// most reuse.
+constexpr int kGroupWaves = 8;
+// The backward's items hold more per head in L2 (Q, dO and the fp32 dQ
+// accumulator): eight waves of heads measured 6% slower than four, which
+// balance its N = 2048 training shape equally well.
+constexpr int kBwdGroupWaves = 4;
 
 struct FwdSched {
   int BH, N, causal, grid;
@@ -104,7 +111,7 @@ struct BwdSched {
     causal = is_causal;
     grid = grid_size;
     n_blk = (N + 127) / 128;
-    int g = (causal ? kGroupWaves : 1) * grid / n_blk;
+    int g = (causal ? kBwdGroupWaves : 1) * grid / n_blk;
     if (g < 1) g = 1;
     if (g > BH) g = BH;
     group = g;

@@ -41,9 +41,18 @@ def lib():
                                        i, i, i, lp, i64, i, dp]
         L.oracle_online_normalizer.argtypes = [dp, i, i, dp, dp]
         L.oracle_tile_census.argtypes = [i64, i, i, i, i, i, lp]
+        L.oracle_fwd_w.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_, i, i]
+        L.oracle_fwd_rows_w.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_, i,
+                                        i, lp, i64, i]
+        L.oracle_bwd_w.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i,
+                                   d_, i, i]
+        L.oracle_fwd_tiled_w.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_,
+                                         i, i, i, lp]
         for name in ("oracle_scores", "oracle_probs", "oracle_fwd",
                      "oracle_fwd_rows", "oracle_bwd", "oracle_fwd_tiled",
-                     "oracle_online_normalizer", "oracle_tile_census"):
+                     "oracle_online_normalizer", "oracle_tile_census",
+                     "oracle_fwd_w", "oracle_fwd_rows_w", "oracle_bwd_w",
+                     "oracle_fwd_tiled_w"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -93,45 +102,60 @@ def probs(Q, K, scale, causal=False):
     return P
 
 
-def fwd(Q, K, V, scale, causal=False, nthreads=0):
+def fwd(Q, K, V, scale, causal=False, nthreads=0, window=0):
     """O = softmax(scale*QK^T)V and LSE = m + ln l, row by row ("FlashAttention
-    from scratch", follow-up on the backward pass, for L = m + log l)."""
+    from scratch", follow-up on the backward pass, for L = m + log l).
+    window > 0: the causal sliding window of the "LLM Architecture Refresh
+    [3]" section 5 contrast, query r sees keys r - window + 1 .. r."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     B, H, N, d = _shape4(Q)
     O = np.empty((B, H, N, d))
     LSE = np.empty((B, H, N))
+    if window > 0:
+        _check(lib().oracle_fwd_w(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
+                                  B, H, N, d, float(scale), int(window),
+                                  int(nthreads)), "fwd_w")
+        return O, LSE
     _check(lib().oracle_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                             B, H, N, d, float(scale), int(causal),
                             int(nthreads)), "fwd")
     return O, LSE
 
 
-def fwd_rows(Q, K, V, scale, causal, rows, nthreads=0):
+def fwd_rows(Q, K, V, scale, causal, rows, nthreads=0, window=0):
     """The forward definition evaluated only at the flat rows
-    (b*H + h)*N + r listed in ``rows``; returns O[len(rows), d], LSE[len]."""
+    (b*H + h)*N + r listed in ``rows``; returns O[len(rows), d], LSE[len].
+    window > 0 selects the causal sliding window (see fwd)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     B, H, N, d = _shape4(Q)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     O = np.empty((rows.size, d))
     LSE = np.empty((rows.size,))
-    _check(lib().oracle_fwd_rows(
+    _check(lib().oracle_fwd_rows_w(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, N, d,
-        float(scale), int(causal),
+        float(scale), int(causal), int(window),
         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), rows.size,
         int(nthreads)), "fwd_rows")
     return O, LSE
 
 
-def bwd(Q, K, V, dO, scale, causal=False, nthreads=0):
+def bwd(Q, K, V, dO, scale, causal=False, nthreads=0, window=0):
     """dQ, dK, dV of the scalar <dO, O>, plus D_r = sum_k p_rk dP_rk ("Flash
     Attention, From First Principles", "The ghost at the door"; "FlashAttention
-    from scratch", follow-up on the backward pass)."""
+    from scratch", follow-up on the backward pass).  window > 0 selects the
+    causal sliding window (see fwd)."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
     B, H, N, d = _shape4(Q)
     dQ = np.empty((B, H, N, d))
     dK = np.empty((B, H, N, d))
     dV = np.empty((B, H, N, d))
     D = np.empty((B, H, N))
+    if window > 0:
+        _check(lib().oracle_bwd_w(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ),
+                                  _ptr(dK), _ptr(dV), _ptr(D), B, H, N, d,
+                                  float(scale), int(window), int(nthreads)),
+               "bwd_w")
+        return dQ, dK, dV, D
     _check(lib().oracle_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ),
                             _ptr(dK), _ptr(dV), _ptr(D), B, H, N, d,
                             float(scale), int(causal), int(nthreads)), "bwd")
@@ -158,6 +182,23 @@ def fwd_tiled(Q, K, V, scale, causal, block_q, block_k, flags=0,
         int(trace_bh), int(trace_row), _ptr(trace)), "fwd_tiled")
     used = ~np.isnan(trace[:, 0])
     return O, LSE, tuple(int(c) for c in counters), trace[used]
+
+
+def fwd_tiled_window(Q, K, V, scale, window, block_q, block_k):
+    """fwd_tiled for the causal sliding window: key blocks entirely older than
+    a query block's window are skipped as well as future ones.  Returns
+    (O, LSE, counters)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N, d = _shape4(Q)
+    O = np.empty((B, H, N, d))
+    LSE = np.empty((B, H, N))
+    counters = np.zeros(3, dtype=np.int64)
+    _check(lib().oracle_fwd_tiled_w(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, N, d,
+        float(scale), int(window), int(block_q), int(block_k),
+        counters.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong))),
+        "fwd_tiled_w")
+    return O, LSE, tuple(int(c) for c in counters)
 
 
 def online_normalizer(x, block):

@@ -20,7 +20,11 @@
  *
  * Definition ([FP] "What is attention?", Stop 1-3; [LAR] section 4 applies the
  * scale; [FAS] follow-up "How do you implement the backward pass"):
- *   s_rk  = scale * <q_r, k_k>            (k > r is -inf when causal)
+ *   s_rk  = scale * <q_r, k_k>            (k > r is -inf when causal; with a
+ *                                          sliding window of w keys, also
+ *                                          k < r - w + 1: [LAR] section 5's
+ *                                          contrast, "each query attends only
+ *                                          to the last w keys")
  *   m_r   = max_k s_rk
  *   l_r   = sum_k exp(s_rk - m_r)
  *   p_rk  = exp(s_rk - m_r) / l_r
@@ -112,13 +116,22 @@ static double dot(const double *a, const double *b, int d) {
     return acc;
 }
 
-/* Fills s[0..N) with the scaled scores of row r; keys after r are -inf when
- * causal ([LAR] section 5: scores above the diagonal forced to -inf). */
+/* Is key k visible to query r?  Causal: k <= r ([LAR] section 5: scores
+ * above the diagonal forced to -inf).  A sliding window of w > 0 keys (which
+ * implies causal) also hides k < r - w + 1 ([LAR] section 5, the
+ * sliding-window contrast: the query and the w - 1 keys before it). */
+static int visible(int causal, int window, int r, int k) {
+    if (window > 0) return k <= r && k >= r - window + 1;
+    return !causal || k <= r;
+}
+
+/* Fills s[0..N) with the scaled scores of row r; invisible keys are -inf. */
 static void row_scores(const double *Qh, const double *Kh, int N, int d,
-                       double scale, int causal, int r, double *s) {
+                       double scale, int causal, int window, int r,
+                       double *s) {
     const double *q = Qh + (i64)r * d;
     for (int k = 0; k < N; ++k) {
-        if (causal && k > r)
+        if (!visible(causal, window, r, k))
             s[k] = -INFINITY;
         else
             s[k] = scale * dot(q, Kh + (i64)k * d, d);
@@ -144,10 +157,10 @@ static double row_softmax(const double *s, double *p, int N, double *l_out) {
 
 /* o_r = sum_k p_k v_k and LSE_r = m + ln l for one row. */
 static void attend_row(const double *Qh, const double *Kh, const double *Vh,
-                       int N, int d, double scale, int causal, int r,
-                       double *work, double *o, double *lse) {
+                       int N, int d, double scale, int causal, int window,
+                       int r, double *work, double *o, double *lse) {
     double l;
-    row_scores(Qh, Kh, N, d, scale, causal, r, work);
+    row_scores(Qh, Kh, N, d, scale, causal, window, r, work);
     double m = row_softmax(work, work, N, &l);
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     for (int k = 0; k < N; ++k) {
@@ -168,8 +181,8 @@ int oracle_scores(const double *Q, const double *K, double *S, int B, int H,
     i64 heads = (i64)B * H;
     for (i64 bh = 0; bh < heads; ++bh)
         for (int r = 0; r < N; ++r)
-            row_scores(Q + bh * N * d, K + bh * N * d, N, d, scale, causal, r,
-                       S + (bh * N + r) * N);
+            row_scores(Q + bh * N * d, K + bh * N * d, N, d, scale, causal, 0,
+                       r, S + (bh * N + r) * N);
     return 0;
 }
 
@@ -190,7 +203,7 @@ int oracle_probs(const double *Q, const double *K, double *P, int B, int H,
 typedef struct {
     const double *Q, *K, *V;
     double *O, *LSE;
-    int N, d, causal;
+    int N, d, causal, window;
     double scale;
     const i64 *rows; /* NULL: all rows in order */
 } fwd_ctx;
@@ -204,7 +217,7 @@ static void fwd_range(void *p, i64 begin, i64 end) {
         int r = (int)(flat % c->N);
         i64 off = bh * c->N * c->d;
         attend_row(c->Q + off, c->K + off, c->V + off, c->N, c->d, c->scale,
-                   c->causal, r, work, c->O + i * c->d,
+                   c->causal, c->window, r, work, c->O + i * c->d,
                    c->LSE ? c->LSE + i : NULL);
     }
     free(work);
@@ -214,22 +227,49 @@ int oracle_fwd(const double *Q, const double *K, const double *V, double *O,
                double *LSE, int B, int H, int N, int d, double scale,
                int causal, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !O) return -1;
-    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal, scale, NULL};
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal, 0, scale, NULL};
     parallel_for((i64)B * H * N, nthreads, fwd_range, &c);
     return 0;
 }
+
+/* Causal sliding window of `window` >= 1 keys (query r sees keys
+ * r - window + 1 .. r). */
+int oracle_fwd_w(const double *Q, const double *K, const double *V, double *O,
+                 double *LSE, int B, int H, int N, int d, double scale,
+                 int window, int nthreads) {
+    if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || window < 1) return -1;
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, 1, window, scale, NULL};
+    parallel_for((i64)B * H * N, nthreads, fwd_range, &c);
+    return 0;
+}
+
+int oracle_fwd_rows_w(const double *Q, const double *K, const double *V,
+                      double *O, double *LSE, int B, int H, int N, int d,
+                      double scale, int causal, int window, const i64 *rows,
+                      i64 nrows, int nthreads);
 
 /* rows[i] is a flat row index (b*H + h)*N + r; O is [nrows][d], LSE [nrows]. */
 int oracle_fwd_rows(const double *Q, const double *K, const double *V,
                     double *O, double *LSE, int B, int H, int N, int d,
                     double scale, int causal, const i64 *rows, i64 nrows,
                     int nthreads) {
-    if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || !rows || nrows < 0)
+    return oracle_fwd_rows_w(Q, K, V, O, LSE, B, H, N, d, scale, causal, 0,
+                             rows, nrows, nthreads);
+}
+
+/* As oracle_fwd_rows; window > 0 selects the causal sliding window. */
+int oracle_fwd_rows_w(const double *Q, const double *K, const double *V,
+                      double *O, double *LSE, int B, int H, int N, int d,
+                      double scale, int causal, int window, const i64 *rows,
+                      i64 nrows, int nthreads) {
+    if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || !rows || nrows < 0 ||
+        window < 0)
         return -1;
     i64 total = (i64)B * H * N;
     for (i64 i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total) return -2;
-    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal, scale, rows};
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal || window > 0, window, scale,
+                 rows};
     parallel_for(nrows, nthreads, fwd_range, &c);
     return 0;
 }
@@ -243,7 +283,7 @@ int oracle_fwd_rows(const double *Q, const double *K, const double *V,
 typedef struct {
     const double *Q, *K, *V, *dO;
     double *dQ, *dK, *dV, *Dvec;
-    int N, d, causal;
+    int N, d, causal, window;
     double scale;
 } bwd_ctx;
 
@@ -261,7 +301,7 @@ static void bwd_range(void *p, i64 begin, i64 end) {
         memset(dVh, 0, sizeof(double) * (size_t)N * d);
         for (int r = 0; r < N; ++r) {
             double l;
-            row_scores(Qh, Kh, N, d, c->scale, c->causal, r, prob);
+            row_scores(Qh, Kh, N, d, c->scale, c->causal, c->window, r, prob);
             row_softmax(prob, prob, N, &l);
             const double *dOr = dOh + (i64)r * d;
             const double *qr = Qh + (i64)r * d;
@@ -298,7 +338,20 @@ int oracle_bwd(const double *Q, const double *K, const double *V,
                int causal, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !dO || !dQ || !dK || !dV)
         return -1;
-    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, causal, scale};
+    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, causal, 0, scale};
+    parallel_for((i64)B * H, nthreads, bwd_range, &c);
+    return 0;
+}
+
+/* Backward of the causal sliding window of `window` >= 1 keys. */
+int oracle_bwd_w(const double *Q, const double *K, const double *V,
+                 const double *dO, double *dQ, double *dK, double *dV,
+                 double *Dvec, int B, int H, int N, int d, double scale,
+                 int window, int nthreads) {
+    if (bad_shape(B, H, N, d) || !Q || !K || !V || !dO || !dQ || !dK || !dV ||
+        window < 1)
+        return -1;
+    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, 1, window, scale};
     parallel_for((i64)B * H, nthreads, bwd_range, &c);
     return 0;
 }
@@ -317,15 +370,18 @@ int oracle_bwd(const double *Q, const double *K, const double *V,
  * that row's running (m, l, o[0..d)) is appended: (2+d) doubles per block,
  * at most ceil(N/block_k) blocks.
  * flags: ORACLE_PLANT_NO_RESCALE drops the rebase of l and o (the mistake the
- * [FAS] worked example warns about); only the negative-control test sets it. */
-int oracle_fwd_tiled(const double *Q, const double *K, const double *V,
+ * [FAS] worked example warns about); only the negative-control test sets it.
+ * window > 0 selects the causal sliding window: tiles whose last key is
+ * older than the block's first query's window are skipped too. */
+static int fwd_tiled(const double *Q, const double *K, const double *V,
                      double *O, double *LSE, int B, int H, int N, int d,
-                     double scale, int causal, int block_q, int block_k,
-                     int flags, i64 *counters, i64 trace_bh, int trace_row,
-                     double *trace) {
+                     double scale, int causal, int window, int block_q,
+                     int block_k, int flags, i64 *counters, i64 trace_bh,
+                     int trace_row, double *trace) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || block_q < 1 ||
-        block_k < 1)
+        block_k < 1 || window < 0)
         return -1;
+    if (window > 0) causal = 1;
     i64 heads = (i64)B * H;
     i64 flops = 0, computed = 0, skipped = 0;
     double *m = (double *)malloc(sizeof(double) * (size_t)block_q);
@@ -345,18 +401,19 @@ int oracle_fwd_tiled(const double *Q, const double *K, const double *V,
             }
             for (int j = 0; j < N; j += block_k) {
                 int cols = (N - j < block_k) ? N - j : block_k;
-                if (causal && j > i + rows - 1) {
+                if ((causal && j > i + rows - 1) ||
+                    (window > 0 && j + cols - 1 < i - window + 1)) {
                     skipped += 1;
                     continue;
                 }
                 computed += 1;
                 flops += 2 * (2 * (i64)rows * cols * d);
-                /* score tile, with the causal mask inside diagonal tiles */
+                /* score tile, with the mask inside the tiles it cuts */
                 for (int a = 0; a < rows; ++a)
                     for (int b = 0; b < cols; ++b) {
                         int qi = i + a, kj = j + b;
                         sc[(i64)a * block_k + b] =
-                            (causal && kj > qi)
+                            !visible(causal, window, qi, kj)
                                 ? -INFINITY
                                 : scale * dot(Qh + (i64)qi * d,
                                               Kh + (i64)kj * d, d);
@@ -409,6 +466,24 @@ int oracle_fwd_tiled(const double *Q, const double *K, const double *V,
         counters[2] = skipped;
     }
     return 0;
+}
+
+int oracle_fwd_tiled(const double *Q, const double *K, const double *V,
+                     double *O, double *LSE, int B, int H, int N, int d,
+                     double scale, int causal, int block_q, int block_k,
+                     int flags, i64 *counters, i64 trace_bh, int trace_row,
+                     double *trace) {
+    return fwd_tiled(Q, K, V, O, LSE, B, H, N, d, scale, causal, 0, block_q,
+                     block_k, flags, counters, trace_bh, trace_row, trace);
+}
+
+int oracle_fwd_tiled_w(const double *Q, const double *K, const double *V,
+                       double *O, double *LSE, int B, int H, int N, int d,
+                       double scale, int window, int block_q, int block_k,
+                       i64 *counters) {
+    if (window < 1) return -1;
+    return fwd_tiled(Q, K, V, O, LSE, B, H, N, d, scale, 1, window, block_q,
+                     block_k, 0, counters, -1, 0, NULL);
 }
 
 /* ------------------------------------------------------------------ */

@@ -345,6 +345,94 @@ def test_equal_keys_backward_closed_forms():
     np.testing.assert_allclose(dV[0, 0], np.tile(dO[0, 0].mean(axis=0), (N, 1)), atol=1e-14)
 
 
+# --- the causal sliding window ("LLM Architecture Refresh [3]", section 5:
+# each query attends only to the last w keys, itself included) ---
+
+def test_window_covering_every_key_is_causal():
+    Q, K, V = (rand4(2, 2, 23, 5, s) for s in (81, 82, 83))
+    Oc, Lc = oracle.fwd(Q, K, V, 0.4, True)
+    for w in (23, 24, 1000):
+        Ow, Lw = oracle.fwd(Q, K, V, 0.4, window=w)
+        # the same terms in the same order: identical
+        assert np.array_equal(Ow, Oc) and np.array_equal(Lw, Lc)
+
+
+def test_window_of_one_returns_own_value_row():
+    Q, K, V = (rand4(1, 3, 11, 4, s) for s in (84, 85, 86))
+    sc = 0.6
+    O, LSE = oracle.fwd(Q, K, V, sc, window=1)
+    np.testing.assert_allclose(O, V, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(LSE, sc * np.sum(Q * K, axis=-1), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("w", [2, 3, 7])
+def test_window_with_constant_scores_averages_the_last_w_values(w):
+    """Q = 0 makes every visible score 0: row r is the plain mean of
+    v_max(0, r-w+1) .. v_r and LSE_r = ln(min(r+1, w))."""
+    N, d = 13, 3
+    Q = np.zeros((1, 1, N, d))
+    K, V = rand4(1, 1, N, d, 87), rand4(1, 1, N, d, 88)
+    O, LSE = oracle.fwd(Q, K, V, 1.0, window=w)
+    for r in range(N):
+        lo = max(0, r - w + 1)
+        np.testing.assert_allclose(O[0, 0, r], V[0, 0, lo:r + 1].mean(axis=0), atol=1e-14)
+        assert abs(LSE[0, 0, r] - math.log(r + 1 - lo)) < 1e-14
+
+
+@pytest.mark.parametrize("N,w,bq,bk", [(37, 11, 8, 5), (64, 16, 16, 16), (50, 1, 7, 9), (40, 33, 8, 8)])
+def test_window_tiled_equals_untiled_and_skips_old_tiles(N, w, bq, bk):
+    Q, K, V = (rand4(1, 2, N, 6, s) for s in (89, 90, 91))
+    O, L = oracle.fwd(Q, K, V, 0.45, window=w)
+    Ot, Lt, (flops, computed, skipped) = oracle.fwd_tiled_window(Q, K, V, 0.45, w, bq, bk)
+    np.testing.assert_allclose(Ot, O, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(Lt, L, rtol=0, atol=1e-13)
+    # brute-force tile census: a tile is needed iff some (query, key) pair in
+    # it is visible, i.e. key <= query and key >= query - w + 1
+    need = 0
+    for i in range(0, N, bq):
+        for j in range(0, N, bk):
+            qs, ks = range(i, min(N, i + bq)), range(j, min(N, j + bk))
+            if any(k <= q and k >= q - w + 1 for q in qs for k in ks):
+                need += 1
+    tiles = -(-N // bq) * -(-N // bk) * 2
+    assert computed == 2 * need and computed + skipped == tiles
+
+
+@pytest.mark.parametrize("N,d,w", [(7, 3, 3), (5, 2, 1), (6, 4, 5)])
+def test_window_gradients_match_central_differences(N, d, w):
+    Q, K, V, dO = (rand4(1, 2, N, d, s) for s in (92, 93, 94, 95))
+    sc = 0.8
+    dQ, dK, dV, D = oracle.bwd(Q, K, V, dO, sc, window=w)
+    O, _ = oracle.fwd(Q, K, V, sc, window=w)
+    np.testing.assert_allclose(D, np.sum(dO * O, axis=-1), rtol=0, atol=1e-13)
+    h = 1e-6
+
+    def loss():
+        Ow, _ = oracle.fwd(Q, K, V, sc, window=w)
+        return float(np.sum(Ow * dO))
+
+    for X, G in ((Q, dQ), (K, dK), (V, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            old = X[idx]
+            X[idx] = old + h
+            fp = loss()
+            X[idx] = old - h
+            fm = loss()
+            X[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.max(np.abs(num - G)) < 1e-7
+
+
+def test_window_rows_equal_full_window_forward():
+    Q, K, V = (rand4(2, 2, 30, 4, s) for s in (96, 97, 98))
+    O, L = oracle.fwd(Q, K, V, 0.5, window=6)
+    rows = [0, 5, 29, 30 + 7, 60 + 29, 90 + 12]
+    Or, Lr = oracle.fwd_rows(Q, K, V, 0.5, True, rows, window=6)
+    np.testing.assert_allclose(Or, O.reshape(-1, 4)[rows], rtol=0, atol=0)
+    np.testing.assert_allclose(Lr, L.reshape(-1)[rows], rtol=0, atol=0)
+
+
 # --- the seeded generator is exact in the oracle's arithmetic ---
 
 def test_bf16_inputs_widen_exactly():

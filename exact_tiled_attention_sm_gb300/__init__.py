@@ -17,10 +17,11 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 FA_BF16, FA_F32 = 0, 1
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
-           "fa_last_device_status",
+EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_fwd_window",
+           "fa_bwd_window", "fa_bwd_noalloc", "fa_last_device_status",
            "fa_status_string", "fa_selftest_wait_timeout",
-           "fa_fwd_schedule_census", "fa_version")
+           "fa_fwd_schedule_census", "fa_fwd_schedule_census_window",
+           "fa_version")
 
 _lib = None
 
@@ -48,6 +49,14 @@ def lib():
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f,
                              i, i, vp, ctypes.c_size_t, vp]
         L.fa_bwd.restype = i
+        L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        L.fa_fwd_window.restype = i
+        L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
+                                    i, f, i, i, vp, ctypes.c_size_t, vp]
+        L.fa_bwd_window.restype = i
+        L.fa_fwd_schedule_census_window.argtypes = [
+            i, i, i, ctypes.POINTER(ctypes.c_longlong)]
+        L.fa_fwd_schedule_census_window.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i,
                                      i, i, f, i, i, vp]
         L.fa_bwd_noalloc.restype = i
@@ -80,6 +89,18 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal, dt,
                         int(causal), dt, workspace, workspace_bytes, stream)
 
 
+def fa_fwd_window(Q, K, V, O, LSE, B, H, N, d, scale, window, dt, stream):
+    return lib().fa_fwd_window(Q, K, V, O, LSE, B, H, N, d, scale, int(window),
+                               dt, stream)
+
+
+def fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, window,
+                  dt, workspace, workspace_bytes, stream):
+    return lib().fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d,
+                               scale, int(window), dt, workspace,
+                               workspace_bytes, stream)
+
+
 def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
                    dt, stream):
     """fa_bwd with the library's own scratch array instead of a workspace, for
@@ -105,6 +126,14 @@ def fa_fwd_schedule_census(N, causal):
     st = lib().fa_fwd_schedule_census(N, int(causal), out)
     if st != FA_OK:
         raise FAError(st, "fa_fwd_schedule_census")
+    return tuple(out)
+
+
+def fa_fwd_schedule_census_window(N, causal, window):
+    out = (ctypes.c_longlong * 3)()
+    st = lib().fa_fwd_schedule_census_window(N, int(causal), int(window), out)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_schedule_census_window")
     return tuple(out)
 
 
@@ -141,8 +170,10 @@ def _stream_ptr(stream):
     return s.cuda_stream
 
 
-def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None):
-    """O, LSE = attention forward of [B, H, N, d] CUDA tensors (bf16 or fp32)."""
+def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None,
+        window=0):
+    """O, LSE = attention forward of [B, H, N, d] CUDA tensors (bf16 or fp32).
+    window > 0: causal sliding window of that many keys (fa_fwd_window)."""
     import torch
     B, H, N, d = q.shape
     dt = _dtype_code(q)
@@ -156,11 +187,16 @@ def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None):
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_tensor(out, (B, H, N, d), "out")
     _check_tensor(lse, (B, H, N), "lse")
-    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                lse.data_ptr(), B, H, N, d, float(scale), causal, dt,
-                _stream_ptr(stream))
+    if window:
+        st = fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                           float(scale), window, dt, _stream_ptr(stream))
+    else:
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr(), B, H, N, d, float(scale), causal, dt,
+                    _stream_ptr(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_fwd")
+        raise FAError(st, "fa_fwd_window" if window else "fa_fwd")
     return out, lse
 
 
@@ -174,8 +210,9 @@ def workspace(B, H, N, d, device=None):
 
 
 def bwd(q, k, v, o, do, lse, scale, causal=False, dq=None, dk=None, dv=None,
-        ws=None, stream=None):
-    """dQ, dK, dV of attention for upstream gradient ``do``."""
+        ws=None, stream=None, window=0):
+    """dQ, dK, dV of attention for upstream gradient ``do``.  window > 0:
+    causal sliding window of that many keys (fa_bwd_window)."""
     import torch
     B, H, N, d = q.shape
     dt = _dtype_code(q)
@@ -186,12 +223,17 @@ def bwd(q, k, v, o, do, lse, scale, causal=False, dq=None, dk=None, dv=None,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     ws = workspace(B, H, N, d, q.device) if ws is None else ws
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                dv.data_ptr(), B, H, N, d, float(scale), causal, dt,
-                ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), B, H, N, d, float(scale))
+    if window:
+        st = fa_bwd_window(*args, window, dt, ws.data_ptr(), ws.numel(),
+                           _stream_ptr(stream))
+    else:
+        st = fa_bwd(*args, causal, dt, ws.data_ptr(), ws.numel(),
+                    _stream_ptr(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_bwd")
+        raise FAError(st, "fa_bwd_window" if window else "fa_bwd")
     return dq, dk, dv
 
 

@@ -121,11 +121,11 @@ fa_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-}  // namespace
-
-FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
-                        float* LSE, int B, int H, int N, int d, float scale,
-                        int causal, fa_dtype dt, void* stream) {
+// window: 0 for none, else >= 1 (a causal sliding window; one covering the
+// whole sequence is the causal case and is run as such).
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
+                   float* LSE, int B, int H, int N, int d, float scale,
+                   int causal, int window, fa_dtype dt, void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, (int)dt);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
@@ -134,7 +134,9 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
   int dev;
   DeviceInfo info;
   if ((st = current_device(&dev, &info)) != FA_OK) return st;
-  const fa::AttnShape s{B, H, N, d, scale, causal ? 1 : 0};
+  if (window >= N) window = 0;  // sees every earlier key: plain causal
+  const fa::AttnShape s{B, H, N, d, scale, (causal || window > 0) ? 1 : 0,
+                        window};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (dt == FA_F32)
     return from_cuda(fa::launch_fwd_f32(
@@ -151,17 +153,35 @@ FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
                                      fa::kWaitLimitNs, cs));
 }
 
+}  // namespace
+
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
+                        float* LSE, int B, int H, int N, int d, float scale,
+                        int causal, fa_dtype dt, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, causal, 0, dt, stream);
+}
+
+FA_API fa_status fa_fwd_window(const void* Q, const void* K, const void* V,
+                               void* O, float* LSE, int B, int H, int N, int d,
+                               float scale, int window, fa_dtype dt,
+                               void* stream) {
+  if (window < 1) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, 1, window, dt, stream);
+}
+
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_shape(B, H, N, d, 1.0f, FA_BF16) != FA_OK) return 0;
   const size_t rows = (size_t)B * H * N;
   return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
 }
 
-FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
-                        const void* O, const void* dO, const float* LSE,
-                        void* dQ, void* dK, void* dV, int B, int H, int N,
-                        int d, float scale, int causal, fa_dtype dt,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, void* dQ, void* dK,
+                   void* dV, int B, int H, int N, int d, float scale,
+                   int causal, int window, fa_dtype dt, void* workspace,
+                   size_t workspace_bytes, void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, (int)dt);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
@@ -174,7 +194,9 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
   int dev;
   DeviceInfo info;
   if ((st = current_device(&dev, &info)) != FA_OK) return st;
-  const fa::AttnShape s{B, H, N, d, scale, causal ? 1 : 0};
+  if (window >= N) window = 0;
+  const fa::AttnShape s{B, H, N, d, scale, (causal || window > 0) ? 1 : 0,
+                        window};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)B * H * N;
   float* Dvec = static_cast<float*>(workspace);
@@ -209,6 +231,28 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
   return from_cuda(fa::launch_dq_convert(s, dQacc, dQ, cs));
 }
 
+}  // namespace
+
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
+                        const void* O, const void* dO, const float* LSE,
+                        void* dQ, void* dK, void* dV, int B, int H, int N,
+                        int d, float scale, int causal, fa_dtype dt,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
+                  0, dt, workspace, workspace_bytes, stream);
+}
+
+FA_API fa_status fa_bwd_window(const void* Q, const void* K, const void* V,
+                               const void* O, const void* dO, const float* LSE,
+                               void* dQ, void* dK, void* dV, int B, int H,
+                               int N, int d, float scale, int window,
+                               fa_dtype dt, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (window < 1) return FA_ERR_INVALID_ARG;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, 1,
+                  window, dt, workspace, workspace_bytes, stream);
+}
+
 FA_API fa_status fa_last_device_status(void* stream) {
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const unsigned int words[3] = {fa::read_status_fwd_tc(cs),
@@ -240,9 +284,14 @@ FA_API fa_status fa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
 }
 
 FA_API fa_status fa_fwd_schedule_census(int N, int causal, long long* out) {
-  if (N < 1 || !out) return FA_ERR_INVALID_ARG;
+  return fa_fwd_schedule_census_window(N, causal, 0, out);
+}
+
+FA_API fa_status fa_fwd_schedule_census_window(int N, int causal, int window,
+                                               long long* out) {
+  if (N < 1 || !out || window < 0) return FA_ERR_INVALID_ARG;
   fa::FwdSched sc;
-  sc.init(1, N, causal ? 1 : 0, 1);
+  sc.init(1, N, causal ? 1 : 0, 1, window < N ? window : 0);
   long long computed = 0;
   for (int q = 0; q < sc.n_q_tiles; ++q) computed += sc.n_kv(q);
   out[0] = computed;
@@ -251,4 +300,4 @@ FA_API fa_status fa_fwd_schedule_census(int N, int causal, long long* out) {
   return FA_OK;
 }
 
-FA_API int fa_version(void) { return 100; }
+FA_API int fa_version(void) { return 200; }

@@ -110,7 +110,8 @@ enum : uint32_t {
 // -LSE*log2(e) per query (-inf past N, so those columns are exactly 0).
 __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
                                        const float* nlse2, int c0, uint32_t pcol,
-                                       int key, bool kvalid, bool diag, int q0,
+                                       int key, bool kvalid, bool diag,
+                                       int window, bool edge, int q0,
                                        float sl2, float (&pr)[64]) {
   uint32_t sr[2][32];
   tmem_ld32(tmem_row + tm_s + 32 * c0, sr[0]);
@@ -136,11 +137,18 @@ __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
       for (int u = 0; u < 4; ++u) o[u] = ex2_approx(o[u]);
     }
   // causal diagonal block: keys after the query are invisible; key rows past
-  // N (ragged last block) are zeroed too (both warp-uniform, rare branches)
+  // N (ragged last block) are zeroed too (warp-uniform, rare branches)
   if (diag) {
 #pragma unroll
     for (int x = 0; x < 64; ++x)
       if (q0 + 32 * c0 + x < key) pr[x] = 0.f;
+  }
+  // sliding window: a query more than window - 1 rows after the key is
+  // past it (only tiles the window's left edge cuts)
+  if (edge) {
+#pragma unroll
+    for (int x = 0; x < 64; ++x)
+      if (q0 + 32 * c0 + x - key >= window) pr[x] = 0.f;
   }
   if (__any_sync(0xffffffffu, !kvalid)) {
 #pragma unroll
@@ -378,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       kv_last = (int)(it & 1);
-      for (int i = sc.q_begin(kb); i < sc.n_blk; ++i) {
+      const int iend = sc.q_end(kb);
+      for (int i = sc.q_begin(kb); i <= iend; ++i) {
         const int s = qcnt % C::QST;
         const uint32_t ph = (qcnt / C::QST) & 1;
         // -LSE*log2(e) and -D*scale of this block's queries (fetched during
@@ -391,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lv[e] = valid ? -lraw[e] * 1.4426950408889634f : -INFINITY;
           dv[e] = valid ? -draw[e] * p.scale : 0.f;
         }
-        if (i + 1 < sc.n_blk)
+        if (i + 1 <= iend)
           fetch_stats(bh, i + 1);
         else if (nbh >= 0)
           fetch_stats(nbh, ni);
@@ -486,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         if (!issue_s(qcnt)) break;
-        for (int i = i0; i < sc.n_blk; ++i) {
+        const int iend = sc.q_end(kb);
+        for (int i = i0; i <= iend; ++i) {
           const int s = qcnt % C::QST;
           if (g > 0) {  // dQ of the previous block has left TMEM
             if (!wait_one(bar(C::B_DQFREE), (g - 1) & 1, abort_flag, lim,
@@ -533,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(bar(C::B_DQFULL));
           // the next block's S^T: its Q/dO stage was refilled after the
           // stage's previous dQ tile had been reduced out, a full block ago
-          if (i + 1 < sc.n_blk && !issue_s(qcnt + 1)) {
+          if (i + 1 <= iend && !issue_s(qcnt + 1)) {
             ok = false;
             break;
           }
@@ -567,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sc.decode(item, bh, kb);
       const int key = kb * 128 + r;
       const bool kvalid = key < N;
-      for (int i = sc.q_begin(kb); i < sc.n_blk; ++i) {
+      const int iend = sc.q_end(kb);
+      for (int i = sc.q_begin(kb); i <= iend; ++i) {
         const int s = qcnt % C::QST;
         if (!wait_warp(bar(C::B_QFULL + s), (qcnt / C::QST) & 1, abort_flag,
                        lim, SITE_S_QFULL) ||
@@ -579,9 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* lse2 = stat(s);
         const int q0 = i * 128;
         const bool diag = sc.causal && i == kb;
+        const bool edge = sc.window_edge(i, kb);
         float pr[64];
         p_half(tmem_row, C::TM_S, lse2, 2 * grp, 64u * grp, key, kvalid, diag,
-               q0, sl2, pr);
+               sc.window, edge, q0, sl2, pr);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::B_PREADY));
@@ -672,7 +684,7 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   const int n_blk = (s.N + 127) / 128;
   const int total = BH * n_blk;
   const int grid = total < num_sms ? total : num_sms;
-  p.sched.init(BH, s.N, s.causal, grid);
+  p.sched.init(BH, s.N, s.causal, grid, s.window);
   bwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, p);
   return cudaGetLastError();

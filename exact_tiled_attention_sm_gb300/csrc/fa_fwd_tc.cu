@@ -84,7 +84,9 @@ enum : uint32_t {
   SITE_ALIGN
 };
 
-template <int D>
+// W: the causal sliding-window variant (compiled separately, so that the
+// plain kernels carry none of its range bookkeeping).
+template <int D, bool W>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
@@ -154,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc.decode(item, bh, pair);
         const int q0 = 2 * pair;
         const bool valid1 = (q0 + 1) < sc.n_q_tiles;
-        const int n_kv = sc.n_kv(valid1 ? q0 + 1 : q0);
+        // key blocks of either query block: kv_lo(q0) .. kv_hi(last)
+        const int jlo = W ? sc.kv_lo(q0) : 0;
+        const int jhi = sc.kv_hi(valid1 ? q0 + 1 : q0);
         if (it > 0 &&
             !wait_one(bar(C::B_QEMPTY), (it - 1) & 1, abort_flag, lim,
                       SITE_P_QEMPTY))
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         c * 64, (q0 + t) * 128, bh);
         last_q = it & 1;
         bool ok = true;
-        for (int j = 0; j < n_kv && ok; ++j) {
+        for (int j = jlo; j <= jhi && ok; ++j) {
           {
             const int s = kcnt % C::KST;
             const uint32_t ph = (kcnt / C::KST) & 1;
@@ -234,13 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         sc.decode(item, bh, pair);
         const int q0 = 2 * pair;
         const bool valid1 = (q0 + 1) < sc.n_q_tiles;
-        const int n_t0 = sc.n_kv(q0);
-        const int n_t1 = valid1 ? sc.n_kv(q0 + 1) : 0;
-        const int n_kv = n_t1 > n_t0 ? n_t1 : n_t0;
+        // key-block range of each query block (tile 1's may start one block
+        // later and ends one later under the causal mask; empty if absent)
+        const int lo0 = W ? sc.kv_lo(q0) : 0, hi0 = sc.kv_hi(q0);
+        const int lo1 = (W && valid1) ? sc.kv_lo(q0 + 1) : 0;
+        const int hi1 = valid1 ? sc.kv_hi(q0 + 1) : -1;
+        const int jlo = lo0, jhi = hi1 > hi0 ? hi1 : hi0;
+        auto in_t = [&](int t, int j) {
+          return t ? (j >= lo1 && j <= hi1) : (j >= lo0 && j <= hi0);
+        };
         bool ok = wait_one(bar(C::B_QFULL), it & 1, abort_flag, lim, SITE_M_QFULL);
         if (!ok) break;
         tc_fence_after();
-        {  // S_t for key block 0
+        {  // S_t for the first key block
           const int s = kcnt % C::KST;
           if (!wait_one(bar(C::B_KFULL + s), (kcnt / C::KST) & 1, abort_flag,
                         lim, SITE_M_KFULL))
@@ -249,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sk = sb + C::OFF_K + s * C::TILE_BYTES;
 #pragma unroll
           for (int t = 0; t < 2; ++t)
-            if ((t ? n_t1 : n_t0) > 0) {
+            if (in_t(t, jlo)) {
               mma_rows_x_rows<D>(tmem + C::TM_S + 128 * t, sQ(t), sk, C::IDESC_S);
               umma_commit(bar(C::B_SFULL + t));
             }
@@ -257,9 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kcnt;
           // the Q tiles are read by S products only: with a single key block
           // they are free for the next item as soon as these complete
-          if (n_kv == 1) umma_commit(bar(C::B_QEMPTY));
+          if (jlo == jhi) umma_commit(bar(C::B_QEMPTY));
         }
-        for (int j = 0; j < n_kv && ok; ++j) {
+        for (int j = jlo; j <= jhi && ok; ++j) {
           const int vs = vcnt % C::VST;
           if (!wait_one(bar(C::B_VFULL + vs), (vcnt / C::VST) & 1, abort_flag,
                         lim, SITE_M_VFULL)) {
@@ -273,20 +283,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool k_ready = false;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            const int nt = t ? n_t1 : n_t0;
-            if (!ok || j >= nt) continue;
-            uint32_t& pc = t ? pcnt1 : pcnt0;
-            if (!wait_one(bar(C::B_PREADY + t), pc & 1, abort_flag, lim,
-                          SITE_M_PREADY)) {
-              ok = false;
-              continue;
+            if (!ok) continue;
+            if (in_t(t, j)) {
+              uint32_t& pc = t ? pcnt1 : pcnt0;
+              if (!wait_one(bar(C::B_PREADY + t), pc & 1, abort_flag, lim,
+                            SITE_M_PREADY)) {
+                ok = false;
+                continue;
+              }
+              ++pc;
+              tc_fence_after();
+              mma_tmem_x_rows(tmem + C::TM_O + D * t, tmem + C::TM_S + 128 * t,
+                              sv, C::IDESC_PV, j > (t ? lo1 : lo0));
+              if (j == (t ? hi1 : hi0)) umma_commit(bar(C::B_ODONE + t));
             }
-            ++pc;
-            tc_fence_after();
-            mma_tmem_x_rows(tmem + C::TM_O + D * t, tmem + C::TM_S + 128 * t,
-                            sv, C::IDESC_PV, j > 0);
-            if (j == nt - 1) umma_commit(bar(C::B_ODONE + t));
-            if (j + 1 < nt) {
+            if (in_t(t, j + 1)) {
               if (!k_ready) {
                 if (!wait_one(bar(C::B_KFULL + ks), (kcnt / C::KST) & 1,
                               abort_flag, lim, SITE_M_KFULL)) {
@@ -308,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // the item's last S products have been issued: the next item's Q
           // tiles may load while its last P V products and epilogue run
-          if (ok && j + 2 == n_kv) umma_commit(bar(C::B_QEMPTY));
+          if (ok && j + 1 == jhi) umma_commit(bar(C::B_QEMPTY));
         }
         if (!ok) break;
         ++it;
@@ -336,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       sc.decode(item, bh, pair);
       const int q = 2 * pair + t;
       if (q >= sc.n_q_tiles) continue;
-      const int nt = sc.n_kv(q);
+      const int jlo = W ? sc.kv_lo(q) : 0, jhi = sc.kv_hi(q);
       const int row = q * 128 + wq * 32 + lane;
       float m = -INFINITY;     // running row maximum of the raw scores
       float mref = -INFINITY;  // exponent reference of l and O_t (log2 units)
       float l = 0.f;
       bool ok = true;
-      for (int j = 0; j < nt; ++j) {
+      for (int j = jlo; j <= jhi; ++j) {
         if (!wait_warp(bar(C::B_SFULL + t), scnt & 1, abort_flag, lim,
                        SITE_S_SFULL)) {
           ok = false;
@@ -368,12 +379,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[64 + i] = __uint_as_float(r2[i]);
           x[96 + i] = __uint_as_float(r3[i]);
         }
-        if (sc.needs_mask(q, j)) {
+        if (sc.needs_mask(q, j) || (W && sc.window_edge(q, j))) {
+          // visible keys: lo_k <= key < lim_k (the window's left edge, the
+          // diagonal, the end of the sequence)
           const int k0 = j * 128;
-          const int lim_k = sc.causal ? min(row + 1, sc.N) : sc.N;  // keys < lim_k visible
+          const int lim_k = sc.causal ? min(row + 1, sc.N) : sc.N;
+          if constexpr (W) {
+            const int lo_k = row - sc.window + 1;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (k0 + i >= lim_k) x[i] = -INFINITY;
+            for (int i = 0; i < 128; ++i)
+              if (k0 + i >= lim_k || k0 + i < lo_k) x[i] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i)
+              if (k0 + i >= lim_k) x[i] = -INFINITY;
+          }
         }
         // Row maximum of the raw scores (scale > 0 commutes with max): eight
         // independent chains of three-input maxima, then a short tree.
@@ -402,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // did).  O's first 64 columns are requested (always, which keeps the
         // register allocation free of branches) before the last quarter of
         // the exponentials, so that their TMEM latency hides behind it.
-        const bool resc = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+        const bool resc = j > jlo && __any_sync(0xffffffffu, alpha != 1.f);
         uint32_t oa[2][32];
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
@@ -511,14 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool W>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
                    float* LSE, int num_sms, uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D>;
   static bool attr_done = false;  // per process; same value on every device
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(
-        fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        fwd_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -530,11 +550,11 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   p.wait_limit_ns = lim;
   const int BH = s.B * s.H;
   FwdSched probe;
-  probe.init(BH, s.N, s.causal, num_sms);
+  probe.init(BH, s.N, s.causal, num_sms, s.window);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
-  p.sched.init(BH, s.N, s.causal, grid);
-  fwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps.q, maps.k,
-                                                             maps.v, p);
+  p.sched.init(BH, s.N, s.causal, grid, s.window);
+  fwd_kernel<D, W><<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps.q, maps.k,
+                                                                maps.v, p);
   return cudaGetLastError();
 }
 
@@ -543,9 +563,12 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
 cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
                           float* LSE, int num_sms, uint64_t wait_limit_ns,
                           cudaStream_t stream) {
+  const bool w = s.window > 0;
   if (s.d == 64)
-    return fwdtc::launch<64>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
-  return fwdtc::launch<128>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+    return w ? fwdtc::launch<64, true>(s, maps, O, LSE, num_sms, wait_limit_ns, stream)
+             : fwdtc::launch<64, false>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+  return w ? fwdtc::launch<128, true>(s, maps, O, LSE, num_sms, wait_limit_ns, stream)
+           : fwdtc::launch<128, false>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
 }
 
 FA_DEFINE_STATUS_READER(read_status_fwd_tc)

@@ -11,6 +11,7 @@ struct AttnShape {
   int B, H, N, d;
   float scale;
   int causal;
+  int window = 0;  // > 0: causal sliding window of this many keys
 };
 
 // TMA descriptors (built by fa_api.cu): the bf16 [B*H, N, d] tensors with

@@ -2,11 +2,15 @@
 //
 // A work item is one head (b, h) and one pair of consecutive 128-row query
 // blocks (rows [256*pair, 256*pair + 256)).  For query block q, the key
-// blocks visited are j = 0 .. n_kv(q)-1 with n_kv(q) = q + 1 under the
-// causal mask and ceil(N/128) otherwise: a key block whose first key lies
-// after the query block's last row is never loaded or multiplied ("LLM
-// Architecture Refresh [3]", section 7), and only the diagonal block (and a
-// ragged last block) is masked element by element.
+// blocks visited are j = kv_lo(q) .. kv_hi(q): all of them without a mask;
+// up to the diagonal (kv_hi = q) under the causal mask, where a key block
+// whose first key lies after the query block's last row is never loaded or
+// multiplied ("LLM Architecture Refresh [3]", section 7); and with a sliding
+// window of w keys (query r sees keys r-w+1 .. r, section 5's contrast) also
+// from the block holding the first row's oldest visible key, so blocks that
+// are entirely too old are skipped the same way.  Only the blocks a mask
+// edge cuts (the diagonal, the window's left edge, a ragged last block) are
+// masked element by element.
 //
 // Balance.  Causal items cost in proportion to (pair + 1), so within a group
 // of heads items are listed heaviest first, and a persistent grid takes the
@@ -34,13 +38,16 @@ constexpr int kGroupWaves = 8;
 constexpr int kBwdGroupWaves = 4;
 
 struct FwdSched {
-  int BH, N, causal, grid;
+  int BH, N, causal, window, grid;
   int n_q_tiles, n_pairs, n_kv_total, group, total_items;
 
-  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size) {
+  // window > 0: causal sliding window of `window` keys (implies causal).
+  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size,
+                                int win = 0) {
     BH = bh;
     N = n;
-    causal = is_causal;
+    window = win > 0 ? win : 0;
+    causal = (is_causal || window > 0) ? 1 : 0;
     grid = grid_size;
     n_q_tiles = (N + 127) / 128;
     n_kv_total = n_q_tiles;
@@ -83,32 +90,49 @@ struct FwdSched {
     bh = g * group + r % gs;
   }
 
-  // Key blocks visited by query block q (q < n_q_tiles).
-  __host__ __device__ int n_kv(int q) const {
-    if (!causal) return n_kv_total;
-    return q + 1 < n_kv_total ? q + 1 : n_kv_total;
+  // First and last key block visited by query block q (q < n_q_tiles).
+  __host__ __device__ int kv_lo(int q) const {
+    if (window == 0) return 0;
+    const int first_key = q * 128 - window + 1;  // oldest key row q*128 sees
+    return first_key <= 0 ? 0 : first_key / 128;
   }
+  __host__ __device__ int kv_hi(int q) const {
+    const int n = !causal ? n_kv_total
+                          : (q + 1 < n_kv_total ? q + 1 : n_kv_total);
+    return n - 1;
+  }
+  // Number of key blocks visited by query block q.
+  __host__ __device__ int n_kv(int q) const { return kv_hi(q) - kv_lo(q) + 1; }
 
-  // Does key block j of query block q need an element mask?
+  // Does key block j of query block q need an element mask for the causal
+  // diagonal or the ragged end?  (window_edge: for the window's left edge.)
   __host__ __device__ bool needs_mask(int q, int j) const {
     return (causal && j == q) || (j == n_kv_total - 1 && (N & 127) != 0);
+  }
+  __host__ __device__ bool window_edge(int q, int j) const {
+    return window > 0 && j * 128 < q * 128 + 128 - window;
   }
 };
 
 // The backward kernel's scheduler: a work item is one head and one 128-key
 // block kb; the CTA keeps K_kb and V_kb resident and walks the query blocks
-// i = q_begin(kb) .. n_blk-1 (i >= kb under the causal mask: query blocks that
-// lie entirely before the key block see none of it).  Causal cost is
+// i = q_begin(kb) .. q_end(kb) (i >= kb under the causal mask: query blocks
+// that lie entirely before the key block see none of it; with a sliding
+// window also i <= the block of the last query whose window still reaches
+// the key block's last key).  Causal cost is
 // proportional to n_blk - kb, so items are listed kb-ascending (heaviest
 // first) inside head groups, and taken in snake waves as in FwdSched.
 struct BwdSched {
-  int BH, N, causal, grid;
+  int BH, N, causal, window, grid;
   int n_blk, group, total_items;
 
-  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size) {
+  // window > 0: causal sliding window of `window` keys (implies causal).
+  __host__ __device__ void init(int bh, int n, int is_causal, int grid_size,
+                                int win = 0) {
     BH = bh;
     N = n;
-    causal = is_causal;
+    window = win > 0 ? win : 0;
+    causal = (is_causal || window > 0) ? 1 : 0;
     grid = grid_size;
     n_blk = (N + 127) / 128;
     int g = (causal ? kBwdGroupWaves : 1) * grid / n_blk;
@@ -147,6 +171,18 @@ struct BwdSched {
   }
 
   __host__ __device__ int q_begin(int kb) const { return causal ? kb : 0; }
+  // Last query block that sees any key of block kb (inclusive).
+  __host__ __device__ int q_end(int kb) const {
+    if (window == 0) return n_blk - 1;
+    const int last_q = kb * 128 + 127 + window - 1;  // its window's newest row
+    const int blk = last_q / 128;
+    return blk < n_blk - 1 ? blk : n_blk - 1;
+  }
+  // Does query block i see some key of block kb only partly (the window's
+  // left edge cuts the tile)?
+  __host__ __device__ bool window_edge(int i, int kb) const {
+    return window > 0 && (i - kb) * 128 + 127 >= window;
+  }
 };
 
 }  // namespace fa

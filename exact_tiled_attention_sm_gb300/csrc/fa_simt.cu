@@ -46,7 +46,8 @@ template <int D>
 __global__ void __launch_bounds__(128)
     fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                    const float* __restrict__ V, float* __restrict__ O,
-                   float* __restrict__ LSE, int N, float scale, int causal) {
+                   float* __restrict__ LSE, int N, float scale, int causal,
+                   int window) {
   constexpr int LD = D + 1;  // padded: lane k reads row k without conflicts
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][D]
@@ -82,7 +83,8 @@ __global__ void __launch_bounds__(128)
 #pragma unroll 16
       for (int c = 0; c < D; ++c) s = fmaf(sQ[lr * D + c], sK[lane * LD + c], s);
       s *= scale;
-      if (key >= N || (causal && key > row)) s = -INFINITY;
+      if (key >= N || (causal && key > row) || (window > 0 && row - key >= window))
+        s = -INFINITY;
       const float m_new = fmaxf(m[rr], warp_max(s));
       const float corr = (m_new == -INFINITY) ? 1.f : expf(m[rr] - m_new);
       const float pr = (s == -INFINITY) ? 0.f : expf(s - m_new);
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(128)
                         const float* __restrict__ V, const float* __restrict__ dO,
                         const float* __restrict__ LSE, const float* __restrict__ Dv,
                         float* __restrict__ dK, float* __restrict__ dV, int N,
-                        float scale, int causal) {
+                        float scale, int causal, int window) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][LD]
@@ -158,7 +160,8 @@ __global__ void __launch_bounds__(128)
         s = fmaf(sQ[lane * LD + c], sK[lk * D + c], s);
         dp = fmaf(sdO[lane * LD + c], sV[lk * D + c], dp);
       }
-      const bool vis = qvalid && key < N && !(causal && key > qrow);
+      const bool vis = qvalid && key < N && !(causal && key > qrow) &&
+                       !(window > 0 && qrow - key >= window);
       const float pr = vis ? expf(s * scale - lse) : 0.f;
       const float ds = pr * (dp - Dq);
 #pragma unroll
@@ -192,7 +195,8 @@ __global__ void __launch_bounds__(128)
     bwd_f32_dq_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                       const float* __restrict__ V, const float* __restrict__ dO,
                       const float* __restrict__ LSE, const float* __restrict__ Dv,
-                      float* __restrict__ dQ, int N, float scale, int causal) {
+                      float* __restrict__ dQ, int N, float scale, int causal,
+                      int window) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][D]
@@ -231,7 +235,8 @@ __global__ void __launch_bounds__(128)
         s = fmaf(sQ[lr * D + c], sK[lane * LD + c], s);
         dp = fmaf(sdO[lr * D + c], sV[lane * LD + c], dp);
       }
-      const bool vis = rvalid && key < N && !(causal && key > row);
+      const bool vis = rvalid && key < N && !(causal && key > row) &&
+                       !(window > 0 && row - key >= window);
       const float pr = vis ? expf(s * scale - lse) : 0.f;
       const float ds = pr * (dp - Dq);
 #pragma unroll
@@ -323,7 +328,7 @@ static cudaError_t fwd_f32_launch(const AttnShape& s, const float* Q,
   if (attr != cudaSuccess) return attr;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
   simt::fwd_f32_kernel<D><<<grid, 128, bytes, stream>>>(Q, K, V, O, LSE, s.N,
-                                                        s.scale, s.causal);
+                                                        s.scale, s.causal, s.window);
   return cudaGetLastError();
 }
 
@@ -340,11 +345,11 @@ static cudaError_t bwd_f32_launch(const AttnShape& s, const float* Q,
   if (a2 != cudaSuccess) return a2;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
   simt::bwd_f32_dkdv_kernel<D><<<grid, 128, bytes, stream>>>(
-      Q, K, V, dO, LSE, Dvec, dK, dV, s.N, s.scale, s.causal);
+      Q, K, V, dO, LSE, Dvec, dK, dV, s.N, s.scale, s.causal, s.window);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   simt::bwd_f32_dq_kernel<D><<<grid, 128, bytes, stream>>>(
-      Q, K, V, dO, LSE, Dvec, dQ, s.N, s.scale, s.causal);
+      Q, K, V, dO, LSE, Dvec, dQ, s.N, s.scale, s.causal, s.window);
   return cudaGetLastError();
 }
 

@@ -76,13 +76,31 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * not matter and on return are unspecified.  Steps: D and zeroed dQ
  * accumulator; per key block, recompute S and P from LSE, dV += P^T dO,
  * dP = dO V^T, dS = P*(dP - D), dK += scale*dS^T Q, dQacc += scale*dS K
- * (fp32 atomics); dQ = dQacc converted to the input dtype.
+ * (fp32 bulk reduce-adds); dQ = dQacc converted to the input dtype.
  * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for a short workspace. */
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
                  const void* dO, const float* LSE, void* dQ, void* dK,
                  void* dV, int B, int H, int N, int d, float scale,
                  int causal, fa_dtype dt, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* Causal sliding window ("LLM Architecture Refresh [3]", section 5, the
+ * sliding-window contrast: each query attends only to the last `window`
+ * keys, itself included), forward and backward.  Key k is visible to query r
+ * iff r - window + 1 <= k <= r.  The arguments and conventions are those of
+ * fa_fwd / fa_bwd with `causal` replaced by `window`; a window of N or more
+ * is the causal computation.  Key blocks entirely older than a query block's
+ * window are skipped like future ones, and only blocks a mask edge cuts are
+ * masked element by element.
+ * Errors: as fa_fwd / fa_bwd, plus FA_ERR_INVALID_ARG for window < 1. */
+fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O,
+                        float* LSE, int B, int H, int N, int d, float scale,
+                        int window, fa_dtype dt, void* stream);
+fa_status fa_bwd_window(const void* Q, const void* K, const void* V,
+                        const void* O, const void* dO, const float* LSE,
+                        void* dQ, void* dK, void* dV, int B, int H, int N,
+                        int d, float scale, int window, fa_dtype dt,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* Size of the device scratch array that fa_bwd_noalloc uses in place of a
  * caller workspace: 64 MiB, statically reserved on every GPU that loads the
@@ -138,6 +156,11 @@ fa_status fa_selftest_wait_timeout(unsigned int limit_us, void* stream);
  * how many work items (pairs of 128-row query blocks) it schedules.  Pure
  * host arithmetic, no GPU needed.  out = {computed, skipped, items}. */
 fa_status fa_fwd_schedule_census(int N, int causal, long long* out);
+
+/* As fa_fwd_schedule_census, with a causal sliding window of `window` keys
+ * when window > 0 (window = 0: the mask selected by `causal`). */
+fa_status fa_fwd_schedule_census_window(int N, int causal, int window,
+                                        long long* out);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int fa_version(void);

@@ -111,6 +111,33 @@ def test_schedule_skips_closed_form_fraction(L, N):
     assert skip * 2 * Bk == (Bk - 1) * Bk * Bk
 
 
+@pytest.mark.parametrize("N,w", [(1, 1), (100, 7), (128, 1), (129, 128), (300, 129),
+                                 (1000, 256), (2048, 64), (4096, 1000), (513, 513),
+                                 (600, 5000)])
+def test_window_schedule_census_matches_tiled_walk(L, N, w):
+    """The sliding window's key-block ranges visit exactly the tiles the
+    oracle's windowed tile loop computes ("LLM Architecture Refresh [3]",
+    sections 5 and 7)."""
+    import numpy as np
+    comp, skip, items = fa.fa_fwd_schedule_census_window(N, 1, w)
+    z = np.zeros((1, 1, N, 1))
+    _, _, (_, oc, os_) = oracle.fwd_tiled_window(z, z, z, 1.0, w, 128, 128)
+    assert (comp, skip) == (oc, os_)
+    assert items == -(-(-(-N // 128)) // 2)
+
+
+def test_window_entry_points_reject_bad_windows(L):
+    a = [16, 16, 16, 16, 16, 1, 1, 16, 64, 0.1]
+    for w in (0, -1, -300):
+        assert fa.fa_fwd_window(*a, w, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    n = fa.fa_bwd_workspace_size(1, 1, 16, 64)
+    b = [256] * 9 + [1, 1, 16, 64, 0.1]
+    for w in (0, -2):
+        assert fa.fa_bwd_window(*b, w, fa.FA_BF16, 256, n, None) == fa.FA_ERR_INVALID_ARG
+    with pytest.raises(fa.FAError):
+        fa.fa_fwd_schedule_census_window(16, 1, -1)
+
+
 def test_library_has_no_oracle_symbols(L):
     """The product library and the oracle share nothing."""
     assert not hasattr(L, "oracle_fwd")

@@ -15,16 +15,17 @@ from tests import helpers as h
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd_bwd(x, scale, causal):
+def run_fwd_bwd(x, scale, causal, window=0):
     q, k, v, do = (x[n].to("cuda") for n in ("Q", "K", "V", "dO"))
     B, H, N, d = q.shape
-    o, lse = fa.fwd(q, k, v, scale, causal)
+    o, lse = fa.fwd(q, k, v, scale, causal, window=window)
     dq, dqb = h.guarded((B, H, N, d), q.dtype)
     dk, dkb = h.guarded((B, H, N, d), q.dtype)
     dv, dvb = h.guarded((B, H, N, d), q.dtype)
     ws = fa.workspace(B, H, N, d)
     ws.fill_(0xFF)  # the workspace's entry contents must not matter
-    fa.bwd(q, k, v, o, do, lse, scale, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+    fa.bwd(q, k, v, o, do, lse, scale, causal, dq=dq, dk=dk, dv=dv, ws=ws,
+           window=window)
     torch.cuda.synchronize()
     assert fa.last_device_status() == fa.FA_OK
     for t, b in ((dq, dqb), (dk, dkb), (dv, dvb)):
@@ -33,9 +34,9 @@ def run_fwd_bwd(x, scale, causal):
     return h.np64(dq), h.np64(dk), h.np64(dv)
 
 
-def oracle_grads(x, scale, causal):
+def oracle_grads(x, scale, causal, window=0):
     Q, K, V, dO = (inputs.to_f64(x[n]) for n in ("Q", "K", "V", "dO"))
-    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, scale, causal)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, scale, causal, window=window)
     return dQ, dK, dV
 
 
@@ -86,6 +87,32 @@ def test_training_workload_sampled_heads():
         ref = oracle_grads(sub, w.scale, True)
         got = (dq[b:b + 1, hh:hh + 1], dk[b:b + 1, hh:hh + 1], dv[b:b + 1, hh:hh + 1])
         check(got, ref, h.TOL_GRAD_REL)
+
+
+# --- causal sliding window ("LLM Architecture Refresh [3]", section 5) ---
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,w", [(7, 2), (128, 1), (129, 64), (300, 5), (300, 129),
+                                 (513, 256), (700, 384)])
+def test_bf16_window_small_ragged(N, w, d):
+    x = h.seeded(1, 2, N, d, seed=700 + N + w + d, dtype="bf16", with_dO=True)
+    sc = d ** -0.5
+    got = run_fwd_bwd(x, sc, True, window=w)
+    check(got, oracle_grads(x, sc, True, window=w), h.TOL_GRAD_REL)
+
+
+@pytest.mark.parametrize("N,w", [(33, 4), (200, 129)])
+def test_f32_window_small(N, w):
+    x = h.seeded(2, 1, N, 64, seed=800 + N + w, dtype="f32", with_dO=True)
+    got = run_fwd_bwd(x, 0.125, True, window=w)
+    errs = check(got, oracle_grads(x, 0.125, True, window=w), h.TOL_GRAD_REL)
+    assert max(errs) < 1e-5
+
+
+def test_window_multi_head_batch():
+    x = h.seeded(2, 3, 1500, 128, seed=901, dtype="bf16", with_dO=True)
+    got = run_fwd_bwd(x, 0.09, True, window=300)
+    check(got, oracle_grads(x, 0.09, True, window=300), h.TOL_GRAD_REL)
 
 
 def test_backward_is_repeatable():

@@ -14,13 +14,14 @@ from tests.conftest import load_golden
 pytestmark = pytest.mark.gpu
 
 
-def run_fwd(x, scale, causal):
-    """Calls fa_fwd with NaN-prefilled, guard-banded O and LSE."""
+def run_fwd(x, scale, causal, window=0):
+    """Calls fa_fwd (fa_fwd_window when window > 0) with NaN-prefilled,
+    guard-banded O and LSE."""
     q, k, v = (x[n].to("cuda") for n in ("Q", "K", "V"))
     B, H, N, d = q.shape
     o, ob = h.guarded((B, H, N, d), q.dtype)
     lse, lb = h.guarded((B, H, N), torch.float32)
-    fa.fwd(q, k, v, scale, causal, out=o, lse=lse)
+    fa.fwd(q, k, v, scale, causal, out=o, lse=lse, window=window)
     torch.cuda.synchronize()
     assert fa.last_device_status() == fa.FA_OK
     assert h.guards_intact(ob) and h.guards_intact(lb), "write outside O/LSE"
@@ -107,12 +108,12 @@ def test_bf16_large_logits_stay_finite():
     assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
 
 
-def _sampled_parity(w, causal, per_head=48):
+def _sampled_parity(w, causal, per_head=48, window=0):
     x = inputs.workload_inputs(w, with_dO=False)
-    o, lse = run_fwd(x, w.scale, causal)
+    o, lse = run_fwd(x, w.scale, causal, window)
     rows = inputs.sample_rows(w.B, w.H, w.N, per_head=per_head, seed=w.seed).numpy()
     Q, K, V = (inputs.to_f64(x[n]) for n in ("Q", "K", "V"))
-    O, L = oracle.fwd_rows(Q, K, V, w.scale, causal, rows)
+    O, L = oracle.fwd_rows(Q, K, V, w.scale, causal, rows, window=window)
     og = o.reshape(-1, w.d)[rows]
     lg = lse.reshape(-1)[rows]
     return h.max_abs(og, O), h.max_abs(lg, L)
@@ -128,6 +129,57 @@ def test_workload_full_size_sampled(name, causal):
 @pytest.mark.parametrize("name", ["long_ctx_8k", "long_ctx_16k", "long_ctx_32k"])
 def test_long_context_sampled(name):
     eo, el = _sampled_parity(inputs.WORKLOADS[name], True, per_head=24)
+    assert eo <= h.TOL_O_BF16 and el <= h.TOL_LSE_BF16, (eo, el)
+
+
+# --- causal sliding window ("LLM Architecture Refresh [3]", section 5) ---
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,w", [(7, 1), (128, 1), (128, 64), (129, 128), (129, 129),
+                                 (300, 16), (300, 129), (300, 256), (513, 200),
+                                 (513, 384), (1000, 127)])
+def test_bf16_window_small_ragged(N, w, d):
+    x = h.seeded(2, 2, N, d, seed=500 + N + w + d, dtype="bf16")
+    sc = d ** -0.5
+    o, lse = run_fwd(x, sc, True, window=w)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), sc, window=w)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("N,w", [(7, 2), (7, 3), (300, 5), (129, 4)])
+def test_bf16_tiny_window(N, w):
+    """Windows of a few keys: O is then close to single value rows, so V is
+    scaled by 1/4 to keep |O| < 1, where the bf16 output's own rounding stays
+    well inside the 1e-2 bound (with |O| near 4 a half ulp alone is 0.008)."""
+    x = h.seeded(1, 2, N, 128, seed=550 + N + w, dtype="bf16")
+    x["V"] = (x["V"].float() * 0.25).to(torch.bfloat16)
+    o, lse = run_fwd(x, 0.0884, True, window=w)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 0.0884, window=w)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("N,w", [(64, 1), (200, 17), (320, 129)])
+def test_f32_window_small(N, w):
+    x = h.seeded(1, 3, N, 128, seed=600 + N + w, dtype="f32")
+    o, lse = run_fwd(x, 0.125, True, window=w)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 0.125, window=w)
+    assert h.max_abs(o, O) <= h.TOL_F32
+    assert h.max_abs(lse, L) <= h.TOL_F32
+
+
+def test_window_covering_the_sequence_is_the_causal_forward():
+    x = h.seeded(2, 3, 700, 128, seed=9, dtype="bf16")
+    oc, lc = run_fwd(x, 0.09, True)
+    for w in (700, 701, 100000):
+        ow, lw = run_fwd(x, 0.09, True, window=w)
+        assert np.array_equal(ow, oc) and np.array_equal(lw, lc)
+
+
+@pytest.mark.parametrize("w", [64, 256, 3000])
+def test_window_long_context_sampled(w):
+    eo, el = _sampled_parity(inputs.WORKLOADS["long_ctx_8k"], True, per_head=24, window=w)
     assert eo <= h.TOL_O_BF16 and el <= h.TOL_LSE_BF16, (eo, el)
 
 

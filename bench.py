@@ -43,6 +43,20 @@ def attn_flops(B, H, N, d, causal, passes):
     return per_head * B * H
 
 
+def window_pairs(N, w):
+    """Visible (query, key) pairs of one head under the causal sliding window
+    of w keys: sum over rows r of min(r + 1, w)."""
+    if w >= N:
+        return N * (N + 1) // 2
+    return w * (w + 1) // 2 + (N - w) * w
+
+
+def window_flops(B, H, N, d, w, passes):
+    """The metric's convention applied to the visible pairs: 4*d per pair for
+    the forward, 14*d for forward+backward."""
+    return (4 if passes == "fwd" else 14) * d * window_pairs(N, w) * B * H
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -337,6 +351,46 @@ def run_ours(args):
                                 "ms": round(ms, 4), "launches": reps}
             launches += reps
         del qf, kf, vf, of, lf
+
+    # --- causal sliding window ("LLM Architecture Refresh [3]", section 5):
+    # a long-context forward with a 4096-key window, and the training step's
+    # shape with a 512-key window (fwd + bwd); FLOPs over the visible pairs
+    window_results = {}
+    for name, win, passes in (("long_ctx_32k", 4096, "fwd"), (WORKLOAD, 512, "fwd+bwd")):
+        wf = inputs.WORKLOADS[name]
+        xf = inputs.workload_inputs(wf, with_dO=(passes != "fwd"))
+        qf, kf, vf = (xf[n].cuda() for n in ("Q", "K", "V"))
+        of = torch.empty_like(qf)
+        lf = torch.empty((wf.B, wf.H, wf.N), dtype=torch.float32, device="cuda")
+        if passes != "fwd":
+            dof = xf["dO"].cuda()
+            dqf, dkf, dvf = torch.empty_like(qf), torch.empty_like(qf), torch.empty_like(qf)
+            wsf = fa.workspace(wf.B, wf.H, wf.N, wf.d)
+
+        def wstep():
+            fa.fwd(qf, kf, vf, wf.scale, True, out=of, lse=lf, window=win)
+            if passes != "fwd":
+                fa.bwd(qf, kf, vf, of, dof, lf, wf.scale, True, dq=dqf, dk=dkf,
+                       dv=dvf, ws=wsf, window=win)
+
+        reps = max(5, args.steps // 4)
+        for _ in range(3):
+            wstep()
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            wstep()
+        b.record(stream)
+        barrier(world)
+        ms = max_over_ranks(a.elapsed_time(b), world) / reps
+        fl = window_flops(wf.B, wf.H, wf.N, wf.d, win, passes)
+        window_results[f"{name}_w{win}_{passes.replace('+', '_')}"] = {
+            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "window": win, "launches": reps * (1 if passes == "fwd" else 4)}
+        launches += reps * (1 if passes == "fwd" else 4)
+        del qf, kf, vf, of, lf
     clocks = sampler.stop()
     st = fa.last_device_status()
     if st != fa.FA_OK:
@@ -351,7 +405,7 @@ def run_ours(args):
     bwd_flops = step_flops - attn_flops(B, H, N, d, causal, "fwd")
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = attn_flops(B, H, N, d, causal, "fwd") / (fwd_ms * 1e-3) / 1e12
-    for r in fwd_results.values():
+    for r in list(fwd_results.values()) + list(window_results.values()):
         r["frac_of_peak"] = round(r["tflops"] / world / peak, 4)
     line = {
         "metric": METRIC,
@@ -393,6 +447,7 @@ def run_ours(args):
             "algorithmic_flops_per_launch": attn_flops(B, H, N, d, causal, "fwd"),
         },
         "fwd": fwd_results,
+        "window": window_results,
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -48,11 +48,23 @@ def lib():
                                    d_, i, i]
         L.oracle_fwd_tiled_w.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_,
                                          i, i, i, lp]
+        u32p, u64 = ctypes.POINTER(ctypes.c_uint32), ctypes.c_uint64
+        L.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        L.oracle_philox4x32_10.restype = None
+        L.oracle_dropout_keep.argtypes = [i, i, i, i, u64,
+                                          ctypes.POINTER(ctypes.c_uint8)]
+        L.oracle_fwd_x.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_, i, i, i,
+                                   u64, i]
+        L.oracle_fwd_rows_x.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, d_, i,
+                                        i, i, u64, lp, i64, i]
+        L.oracle_bwd_x.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i,
+                                   d_, i, i, i, u64, i]
         for name in ("oracle_scores", "oracle_probs", "oracle_fwd",
                      "oracle_fwd_rows", "oracle_bwd", "oracle_fwd_tiled",
                      "oracle_online_normalizer", "oracle_tile_census",
                      "oracle_fwd_w", "oracle_fwd_rows_w", "oracle_bwd_w",
-                     "oracle_fwd_tiled_w"):
+                     "oracle_fwd_tiled_w", "oracle_dropout_keep",
+                     "oracle_fwd_x", "oracle_fwd_rows_x", "oracle_bwd_x"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -102,7 +114,34 @@ def probs(Q, K, scale, causal=False):
     return P
 
 
-def fwd(Q, K, V, scale, causal=False, nthreads=0, window=0):
+def dropout_threshold(p):
+    """t = round(256 p): the byte threshold of the dropout probability p."""
+    t = int(round(256.0 * float(p)))
+    if not 0 <= t <= 255:
+        raise ValueError("dropout probability must lie in [0, 1)")
+    return t
+
+
+def philox4x32_10(ctr, key):
+    """The counter-based generator Philox4x32-10 (Salmon et al., SC'11)."""
+    c = (ctypes.c_uint32 * 4)(*ctr)
+    k = (ctypes.c_uint32 * 2)(*key)
+    out = (ctypes.c_uint32 * 4)()
+    lib().oracle_philox4x32_10(c, k, out)
+    return tuple(out)
+
+
+def dropout_keep(B, H, N, p, seed):
+    """keep[b, h, r, k] in {0, 1} of the dropout reading (see oracle.c)."""
+    keep = np.empty((B, H, N, N), dtype=np.uint8)
+    _check(lib().oracle_dropout_keep(B, H, N, dropout_threshold(p), int(seed),
+                                     keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))),
+           "dropout_keep")
+    return keep
+
+
+def fwd(Q, K, V, scale, causal=False, nthreads=0, window=0, dropout_p=0.0,
+        seed=0):
     """O = softmax(scale*QK^T)V and LSE = m + ln l, row by row ("FlashAttention
     from scratch", follow-up on the backward pass, for L = m + log l).
     window > 0: the causal sliding window of the "LLM Architecture Refresh
@@ -111,6 +150,12 @@ def fwd(Q, K, V, scale, causal=False, nthreads=0, window=0):
     B, H, N, d = _shape4(Q)
     O = np.empty((B, H, N, d))
     LSE = np.empty((B, H, N))
+    if dropout_p:
+        _check(lib().oracle_fwd_x(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
+                                  B, H, N, d, float(scale), int(causal),
+                                  int(window), dropout_threshold(dropout_p),
+                                  int(seed), int(nthreads)), "fwd_x")
+        return O, LSE
     if window > 0:
         _check(lib().oracle_fwd_w(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
                                   B, H, N, d, float(scale), int(window),
@@ -122,7 +167,8 @@ def fwd(Q, K, V, scale, causal=False, nthreads=0, window=0):
     return O, LSE
 
 
-def fwd_rows(Q, K, V, scale, causal, rows, nthreads=0, window=0):
+def fwd_rows(Q, K, V, scale, causal, rows, nthreads=0, window=0, dropout_p=0.0,
+             seed=0):
     """The forward definition evaluated only at the flat rows
     (b*H + h)*N + r listed in ``rows``; returns O[len(rows), d], LSE[len].
     window > 0 selects the causal sliding window (see fwd)."""
@@ -131,15 +177,16 @@ def fwd_rows(Q, K, V, scale, causal, rows, nthreads=0, window=0):
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     O = np.empty((rows.size, d))
     LSE = np.empty((rows.size,))
-    _check(lib().oracle_fwd_rows_w(
+    _check(lib().oracle_fwd_rows_x(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, N, d,
-        float(scale), int(causal), int(window),
-        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), rows.size,
-        int(nthreads)), "fwd_rows")
+        float(scale), int(causal), int(window), dropout_threshold(dropout_p),
+        int(seed), rows.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)),
+        rows.size, int(nthreads)), "fwd_rows")
     return O, LSE
 
 
-def bwd(Q, K, V, dO, scale, causal=False, nthreads=0, window=0):
+def bwd(Q, K, V, dO, scale, causal=False, nthreads=0, window=0, dropout_p=0.0,
+        seed=0):
     """dQ, dK, dV of the scalar <dO, O>, plus D_r = sum_k p_rk dP_rk ("Flash
     Attention, From First Principles", "The ghost at the door"; "FlashAttention
     from scratch", follow-up on the backward pass).  window > 0 selects the
@@ -150,6 +197,13 @@ def bwd(Q, K, V, dO, scale, causal=False, nthreads=0, window=0):
     dK = np.empty((B, H, N, d))
     dV = np.empty((B, H, N, d))
     D = np.empty((B, H, N))
+    if dropout_p:
+        _check(lib().oracle_bwd_x(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ),
+                                  _ptr(dK), _ptr(dV), _ptr(D), B, H, N, d,
+                                  float(scale), int(causal), int(window),
+                                  dropout_threshold(dropout_p), int(seed),
+                                  int(nthreads)), "bwd_x")
+        return dQ, dK, dV, D
     if window > 0:
         _check(lib().oracle_bwd_w(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ),
                                   _ptr(dK), _ptr(dV), _ptr(D), B, H, N, d,

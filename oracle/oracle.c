@@ -38,6 +38,18 @@
  *   dK_k  = scale * sum_r dS_rk q_r
  *   dV_k  = sum_r p_rk dO_r
  *
+ * Dropout (the reading of the pages' "algorithm 2's extra lines", [FP]
+ * "What's left out"): after the softmax, p_rk is replaced by p_rk * M_rk with
+ * M_rk = keep_rk * 256 / (256 - t), keep_rk in {0, 1}, so O = (P o M) V while
+ * LSE stays that of the undropped row.  Then D_r = sum_k p_rk M_rk dP_rk
+ * (still <dO_r, o_r>), dS_rk = p_rk (M_rk dP_rk - D_r), dV_k = sum_r p_rk M_rk
+ * dO_r.  keep_rk comes from the counter-based generator Philox4x32-10
+ * (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2,
+ * 3", SC'11): key = (seed low word, seed high word), counter = (k/4, r/4,
+ * head, 0); of the 16 output bytes, byte (k mod 4) of word (r mod 4) is the
+ * one of (r, k), and keep_rk = (byte >= t).  t = round(256 * dropout
+ * probability) in 0..255.
+ *
  * Every function returns 0 on success and a negative number on bad arguments.
  * Parity pins for every exported function live in tests/test_oracle_pins.py.
  */
@@ -106,6 +118,54 @@ static int bad_shape(int B, int H, int N, int d) {
 }
 
 /* ------------------------------------------------------------------ */
+/* Philox4x32-10, written from its published definition: ten rounds of two
+ * 32x32->64-bit products (multipliers 0xD2511F53 and 0xCD9E8D57) whose
+ * halves are crossed and xored with the key, the key advancing by the Weyl
+ * constants 0x9E3779B9 and 0xBB67AE85 between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
+                          uint32_t out[4]) {
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* Dropout decision for (head bh, query r, key k); see the header comment. */
+static int drop_keep(uint64_t seed, i64 bh, int r, int k, int t) {
+    uint32_t ctr[4] = {(uint32_t)(k >> 2), (uint32_t)(r >> 2), (uint32_t)bh, 0};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    int byte = (int)((out[r & 3] >> (8 * (k & 3))) & 0xFFu);
+    return byte >= t;
+}
+
+/* keep[bh][r][k] as bytes (0/1) for t in 0..255; pins and tests only. */
+int oracle_dropout_keep(int B, int H, int N, int t, uint64_t seed,
+                        uint8_t *keep) {
+    if (B < 1 || H < 1 || N < 1 || t < 0 || t > 255 || !keep) return -1;
+    for (i64 bh = 0; bh < (i64)B * H; ++bh)
+        for (int r = 0; r < N; ++r)
+            for (int k = 0; k < N; ++k)
+                keep[(bh * N + r) * N + k] = (uint8_t)drop_keep(seed, bh, r, k, t);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Scores and probabilities of one query row, straight from the definition
  * ([FP] Stop 1 and Stop 2.5: subtract the row max, exponentiate, divide by
  * the sum).  s and p are caller buffers of N doubles. */
@@ -155,16 +215,29 @@ static double row_softmax(const double *s, double *p, int N, double *l_out) {
     return m;
 }
 
-/* o_r = sum_k p_k v_k and LSE_r = m + ln l for one row. */
+/* Dropout of one call: t = 0 disables it. */
+typedef struct {
+    int t;
+    uint64_t seed;
+} drop_spec;
+
+/* M_rk of the header comment (1 without dropout). */
+static double drop_factor(const drop_spec *dr, i64 bh, int r, int k) {
+    if (!dr || dr->t == 0) return 1.0;
+    return drop_keep(dr->seed, bh, r, k, dr->t) ? 256.0 / (256 - dr->t) : 0.0;
+}
+
+/* o_r = sum_k p_k M_k v_k and LSE_r = m + ln l for row r of head bh. */
 static void attend_row(const double *Qh, const double *Kh, const double *Vh,
                        int N, int d, double scale, int causal, int window,
-                       int r, double *work, double *o, double *lse) {
+                       const drop_spec *dr, i64 bh, int r, double *work,
+                       double *o, double *lse) {
     double l;
     row_scores(Qh, Kh, N, d, scale, causal, window, r, work);
     double m = row_softmax(work, work, N, &l);
     for (int c = 0; c < d; ++c) o[c] = 0.0;
     for (int k = 0; k < N; ++k) {
-        double pk = work[k];
+        double pk = work[k] * drop_factor(dr, bh, r, k);
         if (pk == 0.0) continue;
         const double *v = Vh + (i64)k * d;
         for (int c = 0; c < d; ++c) o[c] += pk * v[c];
@@ -206,6 +279,7 @@ typedef struct {
     int N, d, causal, window;
     double scale;
     const i64 *rows; /* NULL: all rows in order */
+    drop_spec drop;
 } fwd_ctx;
 
 static void fwd_range(void *p, i64 begin, i64 end) {
@@ -217,7 +291,7 @@ static void fwd_range(void *p, i64 begin, i64 end) {
         int r = (int)(flat % c->N);
         i64 off = bh * c->N * c->d;
         attend_row(c->Q + off, c->K + off, c->V + off, c->N, c->d, c->scale,
-                   c->causal, c->window, r, work, c->O + i * c->d,
+                   c->causal, c->window, &c->drop, bh, r, work, c->O + i * c->d,
                    c->LSE ? c->LSE + i : NULL);
     }
     free(work);
@@ -227,7 +301,21 @@ int oracle_fwd(const double *Q, const double *K, const double *V, double *O,
                double *LSE, int B, int H, int N, int d, double scale,
                int causal, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !O) return -1;
-    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal, 0, scale, NULL};
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal, 0, scale, NULL, {0, 0}};
+    parallel_for((i64)B * H * N, nthreads, fwd_range, &c);
+    return 0;
+}
+
+/* Every option at once: causal, sliding window (0: none), dropout threshold
+ * t (0: none) and seed.  With t = 0 this is oracle_fwd / oracle_fwd_w. */
+int oracle_fwd_x(const double *Q, const double *K, const double *V, double *O,
+                 double *LSE, int B, int H, int N, int d, double scale,
+                 int causal, int window, int t, uint64_t seed, int nthreads) {
+    if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || window < 0 || t < 0 ||
+        t > 255)
+        return -1;
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, causal || window > 0, window, scale,
+                 NULL, {t, seed}};
     parallel_for((i64)B * H * N, nthreads, fwd_range, &c);
     return 0;
 }
@@ -238,7 +326,7 @@ int oracle_fwd_w(const double *Q, const double *K, const double *V, double *O,
                  double *LSE, int B, int H, int N, int d, double scale,
                  int window, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || window < 1) return -1;
-    fwd_ctx c = {Q, K, V, O, LSE, N, d, 1, window, scale, NULL};
+    fwd_ctx c = {Q, K, V, O, LSE, N, d, 1, window, scale, NULL, {0, 0}};
     parallel_for((i64)B * H * N, nthreads, fwd_range, &c);
     return 0;
 }
@@ -257,19 +345,33 @@ int oracle_fwd_rows(const double *Q, const double *K, const double *V,
                              rows, nrows, nthreads);
 }
 
+int oracle_fwd_rows_x(const double *Q, const double *K, const double *V,
+                      double *O, double *LSE, int B, int H, int N, int d,
+                      double scale, int causal, int window, int t,
+                      uint64_t seed, const i64 *rows, i64 nrows, int nthreads);
+
 /* As oracle_fwd_rows; window > 0 selects the causal sliding window. */
 int oracle_fwd_rows_w(const double *Q, const double *K, const double *V,
                       double *O, double *LSE, int B, int H, int N, int d,
                       double scale, int causal, int window, const i64 *rows,
                       i64 nrows, int nthreads) {
+    return oracle_fwd_rows_x(Q, K, V, O, LSE, B, H, N, d, scale, causal, window,
+                             0, 0, rows, nrows, nthreads);
+}
+
+/* As oracle_fwd_rows with every option (see oracle_fwd_x). */
+int oracle_fwd_rows_x(const double *Q, const double *K, const double *V,
+                      double *O, double *LSE, int B, int H, int N, int d,
+                      double scale, int causal, int window, int t,
+                      uint64_t seed, const i64 *rows, i64 nrows, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !O || !rows || nrows < 0 ||
-        window < 0)
+        window < 0 || t < 0 || t > 255)
         return -1;
     i64 total = (i64)B * H * N;
     for (i64 i = 0; i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= total) return -2;
     fwd_ctx c = {Q, K, V, O, LSE, N, d, causal || window > 0, window, scale,
-                 rows};
+                 rows, {t, seed}};
     parallel_for(nrows, nthreads, fwd_range, &c);
     return 0;
 }
@@ -285,6 +387,7 @@ typedef struct {
     double *dQ, *dK, *dV, *Dvec;
     int N, d, causal, window;
     double scale;
+    drop_spec drop;
 } bwd_ctx;
 
 static void bwd_range(void *p, i64 begin, i64 end) {
@@ -308,7 +411,7 @@ static void bwd_range(void *p, i64 begin, i64 end) {
             double D = 0.0;
             for (int k = 0; k < N; ++k) {
                 dP[k] = dot(dOr, Vh + (i64)k * d, d);
-                D += prob[k] * dP[k];
+                D += prob[k] * drop_factor(&c->drop, bh, r, k) * dP[k];
             }
             if (c->Dvec) c->Dvec[bh * N + r] = D;
             double *dQr = dQh + (i64)r * d;
@@ -316,14 +419,15 @@ static void bwd_range(void *p, i64 begin, i64 end) {
             for (int k = 0; k < N; ++k) {
                 double pk = prob[k];
                 if (pk == 0.0) continue;
-                double dS = pk * (dP[k] - D);
+                double mk = drop_factor(&c->drop, bh, r, k);
+                double dS = pk * (mk * dP[k] - D);
                 const double *kk = Kh + (i64)k * d;
                 double *dKk = dKh + (i64)k * d;
                 double *dVk = dVh + (i64)k * d;
                 for (int i = 0; i < d; ++i) {
                     dQr[i] += c->scale * dS * kk[i];
                     dKk[i] += c->scale * dS * qr[i];
-                    dVk[i] += pk * dOr[i];
+                    dVk[i] += pk * mk * dOr[i];
                 }
             }
         }
@@ -338,7 +442,21 @@ int oracle_bwd(const double *Q, const double *K, const double *V,
                int causal, int nthreads) {
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !dO || !dQ || !dK || !dV)
         return -1;
-    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, causal, 0, scale};
+    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, causal, 0, scale, {0, 0}};
+    parallel_for((i64)B * H, nthreads, bwd_range, &c);
+    return 0;
+}
+
+/* Every option at once (see oracle_fwd_x). */
+int oracle_bwd_x(const double *Q, const double *K, const double *V,
+                 const double *dO, double *dQ, double *dK, double *dV,
+                 double *Dvec, int B, int H, int N, int d, double scale,
+                 int causal, int window, int t, uint64_t seed, int nthreads) {
+    if (bad_shape(B, H, N, d) || !Q || !K || !V || !dO || !dQ || !dK || !dV ||
+        window < 0 || t < 0 || t > 255)
+        return -1;
+    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, causal || window > 0,
+                 window, scale, {t, seed}};
     parallel_for((i64)B * H, nthreads, bwd_range, &c);
     return 0;
 }
@@ -351,7 +469,7 @@ int oracle_bwd_w(const double *Q, const double *K, const double *V,
     if (bad_shape(B, H, N, d) || !Q || !K || !V || !dO || !dQ || !dK || !dV ||
         window < 1)
         return -1;
-    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, 1, window, scale};
+    bwd_ctx c = {Q, K, V, dO, dQ, dK, dV, Dvec, N, d, 1, window, scale, {0, 0}};
     parallel_for((i64)B * H, nthreads, bwd_range, &c);
     return 0;
 }

@@ -433,6 +433,99 @@ def test_window_rows_equal_full_window_forward():
     np.testing.assert_allclose(Lr, L.reshape(-1)[rows], rtol=0, atol=0)
 
 
+# --- dropout (the reading of "algorithm 2's extra lines", "Flash Attention,
+# From First Principles", what is left out): P o M with M = keep * 256/(256-t),
+# keep from Philox4x32-10 over 4x4 (query, key) patches ---
+
+def test_philox_matches_published_known_answers():
+    g = load_golden("philox4x32_10_kat.json")
+    for case in g["cases"]:
+        ctr = [int(x, 16) for x in case["counter"]]
+        key = [int(x, 16) for x in case["key"]]
+        assert oracle.philox4x32_10(ctr, key) == tuple(int(x, 16) for x in case["out"])
+
+
+def test_dropout_patch_layout_and_locality():
+    """keep(r, k) is byte k%4 of word r%4 of the call at counter
+    (k/4, r/4, head, 0); it depends on nothing but (head, r, k, seed)."""
+    seed, p = 0x1234_5678_9ABC_DEF0, 0.3
+    t = oracle.dropout_threshold(p)
+    keep = oracle.dropout_keep(2, 3, 40, p, seed)
+    g = np.random.default_rng(5)
+    for _ in range(50):
+        bh, r, k = int(g.integers(6)), int(g.integers(40)), int(g.integers(40))
+        out = oracle.philox4x32_10((k // 4, r // 4, bh, 0), (seed & 0xFFFFFFFF, seed >> 32))
+        byte = (out[r % 4] >> (8 * (k % 4))) & 0xFF
+        assert keep.reshape(6, 40, 40)[bh, r, k] == (byte >= t)
+    big = oracle.dropout_keep(2, 3, 100, p, seed)
+    assert np.array_equal(big[:, :, :40, :40], keep)
+    other = oracle.dropout_keep(2, 3, 40, p, seed + 1)
+    assert not np.array_equal(other, keep)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.25, 0.5, 0.9])
+def test_dropout_keep_rate(p):
+    keep = oracle.dropout_keep(2, 4, 512, p, 77)
+    q = 1 - oracle.dropout_threshold(p) / 256
+    n = keep.size
+    assert abs(keep.mean() - q) < 5 * math.sqrt(q * (1 - q) / n)
+
+
+def test_dropout_threshold_zero_is_no_dropout():
+    Q, K, V = (rand4(1, 2, 19, 4, s) for s in (101, 102, 103))
+    O0, L0 = oracle.fwd(Q, K, V, 0.5, True)
+    O1, L1 = oracle.fwd(Q, K, V, 0.5, True, dropout_p=0.001, seed=3)  # t = 0
+    assert np.array_equal(O0, O1) and np.array_equal(L0, L1)
+
+
+def test_dropout_keeps_lse_and_is_unbiased():
+    Q, K, V = (rand4(1, 1, 6, 2, s) for s in (104, 105, 106))
+    O, L = oracle.fwd(Q, K, V, 0.7, False)
+    acc = np.zeros_like(O)
+    n = 3000
+    for seed in range(n):
+        Od, Ld = oracle.fwd(Q, K, V, 0.7, False, dropout_p=0.5, seed=seed)
+        assert np.array_equal(Ld, L)  # the normaliser is the undropped row's
+        acc += Od
+    assert np.max(np.abs(acc / n - O)) < 0.06
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 3)])
+def test_dropout_gradients_match_central_differences(causal, window):
+    N, d = 6, 3
+    Q, K, V, dO = (rand4(1, 2, N, d, s) for s in (107, 108, 109, 110))
+    sc, p, seed = 0.8, 0.4, 99
+    dQ, dK, dV, D = oracle.bwd(Q, K, V, dO, sc, causal, window=window, dropout_p=p, seed=seed)
+    O, _ = oracle.fwd(Q, K, V, sc, causal, window=window, dropout_p=p, seed=seed)
+    np.testing.assert_allclose(D, np.sum(dO * O, axis=-1), rtol=0, atol=1e-13)
+    h = 1e-6
+
+    def loss():
+        Od, _ = oracle.fwd(Q, K, V, sc, causal, window=window, dropout_p=p, seed=seed)
+        return float(np.sum(Od * dO))
+
+    for X, G in ((Q, dQ), (K, dK), (V, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            old = X[idx]
+            X[idx] = old + h
+            fp = loss()
+            X[idx] = old - h
+            fm = loss()
+            X[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.max(np.abs(num - G)) < 1e-7
+
+
+def test_dropout_rows_equal_full_forward():
+    Q, K, V = (rand4(2, 2, 30, 4, s) for s in (111, 112, 113))
+    O, L = oracle.fwd(Q, K, V, 0.5, True, dropout_p=0.2, seed=11)
+    rows = [0, 5, 29, 37, 89, 102]
+    Or, Lr = oracle.fwd_rows(Q, K, V, 0.5, True, rows, dropout_p=0.2, seed=11)
+    np.testing.assert_allclose(Or, O.reshape(-1, 4)[rows], rtol=0, atol=0)
+    np.testing.assert_allclose(Lr, L.reshape(-1)[rows], rtol=0, atol=0)
+
+
 # --- the seeded generator is exact in the oracle's arithmetic ---
 
 def test_bf16_inputs_widen_exactly():

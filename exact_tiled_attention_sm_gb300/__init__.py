@@ -18,7 +18,9 @@ FA_BF16, FA_F32 = 0, 1
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_fwd_window",
-           "fa_bwd_window", "fa_bwd_noalloc", "fa_last_device_status",
+           "fa_bwd_window", "fa_fwd_dropout", "fa_bwd_dropout",
+           "fa_dropout_threshold", "fa_dropout_mask", "fa_bwd_noalloc",
+           "fa_last_device_status",
            "fa_status_string", "fa_selftest_wait_timeout",
            "fa_fwd_schedule_census", "fa_fwd_schedule_census_window",
            "fa_version")
@@ -54,6 +56,18 @@ def lib():
         L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i,
                                     i, f, i, i, vp, ctypes.c_size_t, vp]
         L.fa_bwd_window.restype = i
+        u64 = ctypes.c_ulonglong
+        L.fa_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
+                                     f, u64, i, vp]
+        L.fa_fwd_dropout.restype = i
+        L.fa_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i,
+                                     i, i, f, i, i, f, u64, i, vp,
+                                     ctypes.c_size_t, vp]
+        L.fa_bwd_dropout.restype = i
+        L.fa_dropout_threshold.argtypes = [f]
+        L.fa_dropout_threshold.restype = i
+        L.fa_dropout_mask.argtypes = [vp, i, i, i, f, u64, vp]
+        L.fa_dropout_mask.restype = i
         L.fa_fwd_schedule_census_window.argtypes = [
             i, i, i, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_fwd_schedule_census_window.restype = i
@@ -99,6 +113,31 @@ def fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, window,
     return lib().fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d,
                                scale, int(window), dt, workspace,
                                workspace_bytes, stream)
+
+
+def fa_fwd_dropout(Q, K, V, O, LSE, B, H, N, d, scale, causal, window,
+                   dropout_p, seed, dt, stream):
+    return lib().fa_fwd_dropout(Q, K, V, O, LSE, B, H, N, d, scale,
+                                int(causal), int(window), float(dropout_p),
+                                int(seed), dt, stream)
+
+
+def fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
+                   window, dropout_p, seed, dt, workspace, workspace_bytes,
+                   stream):
+    return lib().fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d,
+                                scale, int(causal), int(window),
+                                float(dropout_p), int(seed), dt, workspace,
+                                workspace_bytes, stream)
+
+
+def fa_dropout_threshold(dropout_p):
+    return lib().fa_dropout_threshold(float(dropout_p))
+
+
+def fa_dropout_mask(keep, B, H, N, dropout_p, seed, stream):
+    return lib().fa_dropout_mask(keep, B, H, N, float(dropout_p), int(seed),
+                                 stream)
 
 
 def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
@@ -171,9 +210,11 @@ def _stream_ptr(stream):
 
 
 def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None,
-        window=0):
+        window=0, dropout_p=0.0, seed=0):
     """O, LSE = attention forward of [B, H, N, d] CUDA tensors (bf16 or fp32).
-    window > 0: causal sliding window of that many keys (fa_fwd_window)."""
+    window > 0: causal sliding window of that many keys (fa_fwd_window);
+    dropout_p > 0: attention dropout with the keep mask of ``seed``
+    (fa_fwd_dropout)."""
     import torch
     B, H, N, d = q.shape
     dt = _dtype_code(q)
@@ -187,7 +228,12 @@ def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None,
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check_tensor(out, (B, H, N, d), "out")
     _check_tensor(lse, (B, H, N), "lse")
-    if window:
+    if dropout_p:
+        st = fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                            out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                            float(scale), causal, window, dropout_p, seed, dt,
+                            _stream_ptr(stream))
+    elif window:
         st = fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                            out.data_ptr(), lse.data_ptr(), B, H, N, d,
                            float(scale), window, dt, _stream_ptr(stream))
@@ -196,7 +242,8 @@ def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None,
                     lse.data_ptr(), B, H, N, d, float(scale), causal, dt,
                     _stream_ptr(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_fwd_window" if window else "fa_fwd")
+        raise FAError(st, "fa_fwd_dropout" if dropout_p else
+                      "fa_fwd_window" if window else "fa_fwd")
     return out, lse
 
 
@@ -210,9 +257,10 @@ def workspace(B, H, N, d, device=None):
 
 
 def bwd(q, k, v, o, do, lse, scale, causal=False, dq=None, dk=None, dv=None,
-        ws=None, stream=None, window=0):
+        ws=None, stream=None, window=0, dropout_p=0.0, seed=0):
     """dQ, dK, dV of attention for upstream gradient ``do``.  window > 0:
-    causal sliding window of that many keys (fa_bwd_window)."""
+    causal sliding window of that many keys (fa_bwd_window); dropout_p > 0:
+    the forward's dropout, regenerated from ``seed`` (fa_bwd_dropout)."""
     import torch
     B, H, N, d = q.shape
     dt = _dtype_code(q)
@@ -226,15 +274,31 @@ def bwd(q, k, v, o, do, lse, scale, causal=False, dq=None, dk=None, dv=None,
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
             do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
             dv.data_ptr(), B, H, N, d, float(scale))
-    if window:
+    if dropout_p:
+        st = fa_bwd_dropout(*args, causal, window, dropout_p, seed, dt,
+                            ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    elif window:
         st = fa_bwd_window(*args, window, dt, ws.data_ptr(), ws.numel(),
                            _stream_ptr(stream))
     else:
         st = fa_bwd(*args, causal, dt, ws.data_ptr(), ws.numel(),
                     _stream_ptr(stream))
     if st != FA_OK:
-        raise FAError(st, "fa_bwd_window" if window else "fa_bwd")
+        raise FAError(st, "fa_bwd_dropout" if dropout_p else
+                      "fa_bwd_window" if window else "fa_bwd")
     return dq, dk, dv
+
+
+def dropout_mask(B, H, N, dropout_p, seed, device=None, stream=None):
+    """The keep mask of fa_fwd_dropout as a [B, H, N, N] uint8 CUDA tensor
+    (1 kept, 0 dropped), written by fa_dropout_mask."""
+    import torch
+    keep = torch.empty((B, H, N, N), dtype=torch.uint8, device=device or "cuda")
+    st = fa_dropout_mask(keep.data_ptr(), B, H, N, dropout_p, seed,
+                         _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_dropout_mask")
+    return keep
 
 
 def last_device_status(stream=None):

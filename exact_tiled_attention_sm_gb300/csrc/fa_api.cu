@@ -121,11 +121,32 @@ fa_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Dropout threshold t = round(256 p), ties to even; -1 when p is NaN,
+// negative, or rounds to 256 or more.
+int threshold_of(float p) {
+  if (!(p >= 0.f) || !std::isfinite(p)) return -1;
+  const double t = std::nearbyint(256.0 * (double)p);
+  return t <= 255.0 ? (int)t : -1;
+}
+
+fa::DropSpec drop_spec(int t, unsigned long long seed) {
+  fa::DropSpec d;
+  if (t > 0) {
+    d.t4 = (uint32_t)t * 0x01010101u;
+    d.keep_scale = (float)(256.0 / (double)(256 - t));
+  }
+  d.k0 = (uint32_t)seed;
+  d.k1 = (uint32_t)(seed >> 32);
+  return d;
+}
+
 // window: 0 for none, else >= 1 (a causal sliding window; one covering the
-// whole sequence is the causal case and is run as such).
+// whole sequence is the causal case and is run as such).  drop.t4 = 0: no
+// dropout.
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
                    float* LSE, int B, int H, int N, int d, float scale,
-                   int causal, int window, fa_dtype dt, void* stream) {
+                   int causal, int window, const fa::DropSpec& drop,
+                   fa_dtype dt, void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, (int)dt);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
@@ -136,7 +157,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
   if ((st = current_device(&dev, &info)) != FA_OK) return st;
   if (window >= N) window = 0;  // sees every earlier key: plain causal
   const fa::AttnShape s{B, H, N, d, scale, (causal || window > 0) ? 1 : 0,
-                        window};
+                        window, drop};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (dt == FA_F32)
     return from_cuda(fa::launch_fwd_f32(
@@ -158,7 +179,8 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
 FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O,
                         float* LSE, int B, int H, int N, int d, float scale,
                         int causal, fa_dtype dt, void* stream) {
-  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, causal, 0, dt, stream);
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, causal, 0, fa::DropSpec{},
+                  dt, stream);
 }
 
 FA_API fa_status fa_fwd_window(const void* Q, const void* K, const void* V,
@@ -166,7 +188,37 @@ FA_API fa_status fa_fwd_window(const void* Q, const void* K, const void* V,
                                float scale, int window, fa_dtype dt,
                                void* stream) {
   if (window < 1) return FA_ERR_INVALID_ARG;
-  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, 1, window, dt, stream);
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, 1, window, fa::DropSpec{},
+                  dt, stream);
+}
+
+FA_API int fa_dropout_threshold(float dropout_p) { return threshold_of(dropout_p); }
+
+FA_API fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V,
+                                void* O, float* LSE, int B, int H, int N, int d,
+                                float scale, int causal, int window,
+                                float dropout_p, unsigned long long seed,
+                                fa_dtype dt, void* stream) {
+  const int t = threshold_of(dropout_p);
+  if (window < 0 || t < 0) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, scale, causal, window,
+                  drop_spec(t, seed), dt, stream);
+}
+
+FA_API fa_status fa_dropout_mask(unsigned char* keep, int B, int H, int N,
+                                 float dropout_p, unsigned long long seed,
+                                 void* stream) {
+  const int t = threshold_of(dropout_p);
+  if (!keep || t < 0 || B < 1 || H < 1 || N < 1 || N > 4 * 65535)
+    return FA_ERR_INVALID_ARG;
+  if ((long long)B * H >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo info;
+  fa_status st = current_device(&dev, &info);
+  if (st != FA_OK) return st;
+  fa::AttnShape s{B, H, N, 64, 1.f, 0, 0, drop_spec(t, seed)};
+  return from_cuda(fa::launch_dropout_mask(s, keep,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -180,8 +232,9 @@ namespace {
 fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* LSE, void* dQ, void* dK,
                    void* dV, int B, int H, int N, int d, float scale,
-                   int causal, int window, fa_dtype dt, void* workspace,
-                   size_t workspace_bytes, void* stream) {
+                   int causal, int window, const fa::DropSpec& drop,
+                   fa_dtype dt, void* workspace, size_t workspace_bytes,
+                   void* stream) {
   fa_status st = check_shape(B, H, N, d, scale, (int)dt);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
@@ -196,7 +249,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   if ((st = current_device(&dev, &info)) != FA_OK) return st;
   if (window >= N) window = 0;
   const fa::AttnShape s{B, H, N, d, scale, (causal || window > 0) ? 1 : 0,
-                        window};
+                        window, drop};
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)B * H * N;
   float* Dvec = static_cast<float*>(workspace);
@@ -239,7 +292,7 @@ FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V,
                         int d, float scale, int causal, fa_dtype dt,
                         void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
-                  0, dt, workspace, workspace_bytes, stream);
+                  0, fa::DropSpec{}, dt, workspace, workspace_bytes, stream);
 }
 
 FA_API fa_status fa_bwd_window(const void* Q, const void* K, const void* V,
@@ -250,7 +303,22 @@ FA_API fa_status fa_bwd_window(const void* Q, const void* K, const void* V,
                                size_t workspace_bytes, void* stream) {
   if (window < 1) return FA_ERR_INVALID_ARG;
   return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, 1,
-                  window, dt, workspace, workspace_bytes, stream);
+                  window, fa::DropSpec{}, dt, workspace, workspace_bytes, stream);
+}
+
+FA_API fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V,
+                                const void* O, const void* dO, const float* LSE,
+                                void* dQ, void* dK, void* dV, int B, int H,
+                                int N, int d, float scale, int causal,
+                                int window, float dropout_p,
+                                unsigned long long seed, fa_dtype dt,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  const int t = threshold_of(dropout_p);
+  if (window < 0 || t < 0) return FA_ERR_INVALID_ARG;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
+                  window, drop_spec(t, seed), dt, workspace, workspace_bytes,
+                  stream);
 }
 
 FA_API fa_status fa_last_device_status(void* stream) {
@@ -300,4 +368,4 @@ FA_API fa_status fa_fwd_schedule_census_window(int N, int causal, int window,
   return FA_OK;
 }
 
-FA_API int fa_version(void) { return 200; }
+FA_API int fa_version(void) { return 300; }

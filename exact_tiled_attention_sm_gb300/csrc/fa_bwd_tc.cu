@@ -34,9 +34,18 @@
 // P^T overwrites columns [0,32) (queries 0-63) and [64,96) (queries 64-127)
 // of S^T, each half inside the columns its own warpgroup has already read;
 // dS^T likewise inside dP^T; dQ_i then reuses the dP^T columns.
+//
+// With dropout (the DR variant) the forward's keep mask M (entries 0 or
+// 256/(256 - t)) is regenerated from the same Philox counters: the tensor
+// core gets P o M (zeroed entries; the factor is applied to dV once, in the
+// epilogue), and dS = P * (M dP - D).  Each thread draws the keep bytes of
+// its key row for the 64 queries of its half while it would otherwise wait
+// for the next S^T: one Philox call per lane and 4 x 4 patch, a byte
+// transpose inside the lane and a word transpose across the quad.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "fa_sched.cuh"
 #include "fa_tiles.cuh"
 
@@ -92,6 +101,7 @@ struct Params {
   float scale;
   float scale_log2;
   uint64_t wait_limit_ns;
+  DropSpec drop;  // used by the DR variant only
   BwdSched sched;
 };
 
@@ -102,17 +112,43 @@ enum : uint32_t {
   SITE_M_DOFULL
 };
 
+// Keep words of key row `key` for the 64 queries q_base + (0..63): word c
+// holds the keep bytes (0xFF kept, 0x00 dropped) of queries q_base + 4c +
+// (0..3).  Lane q of a quad (keys 4*(key/4) + 0..3) draws the query patches
+// 4g + q, g = 0..3; each call's words are indexed by query, its bytes by key,
+// so a byte transpose regroups them by key and a quad transpose hands each
+// lane its own key's words.
+__device__ __forceinline__ void key_row_keep_words(uint32_t (&kw)[16],
+                                                   const DropSpec& d, int bh,
+                                                   int key, int q_base, int lane) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const Philox4 o = philox4x32_10((uint32_t)key >> 2,
+                                    ((uint32_t)q_base >> 2) + 4 * g + (uint32_t)(lane & 3),
+                                    (uint32_t)bh, 0u, d.k0, d.k1);
+    uint32_t a[4] = {o.x[0], o.x[1], o.x[2], o.x[3]};
+    byte_transpose(a);
+    quad_transpose(a, lane);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_bytes(a[c], d.t4);
+  }
+}
+
 // One warpgroup's half of the softmax-gradient step for query block i:
 // chunks c0, c0+1 of 32 query columns; thread = key row r (TMEM lane).
 // Phase P (needs only S^T): P^T = 2^(S*scale*log2(e) - LSE*log2(e)), kept in
 // fp32 registers and written to TMEM as bf16 at `pcol` (columns relative to
 // the S^T block, inside the columns this warpgroup has read).  `nlse2` holds
 // -LSE*log2(e) per query (-inf past N, so those columns are exactly 0).
+// DR: TMEM gets P with the dropped entries zeroed (kw: key_row_keep_words);
+// pr keeps the undropped values.
+template <bool DR>
 __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
                                        const float* nlse2, int c0, uint32_t pcol,
                                        int key, bool kvalid, bool diag,
                                        int window, bool edge, int q0,
-                                       float sl2, float (&pr)[64]) {
+                                       float sl2, float (&pr)[64],
+                                       const uint32_t (&kw)[16]) {
   uint32_t sr[2][32];
   tmem_ld32(tmem_row + tm_s + 32 * c0, sr[0]);
   tmem_ld32(tmem_row + tm_s + 32 * (c0 + 1), sr[1]);
@@ -158,7 +194,10 @@ __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
   for (int h = 0; h < 2; ++h) {
     uint32_t pp[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) pp[k] = pack_bf16x2(pr[32 * h + 2 * k], pr[32 * h + 2 * k + 1]);
+    for (int k = 0; k < 16; ++k) {
+      pp[k] = pack_bf16x2(pr[32 * h + 2 * k], pr[32 * h + 2 * k + 1]);
+      if constexpr (DR) pp[k] &= pair_mask(kw[8 * h + (k >> 1)], k);
+    }
     tmem_st16(tmem_row + tm_s + pcol + 16 * h, pp);
   }
 }
@@ -166,12 +205,14 @@ __device__ __forceinline__ void p_half(uint32_t tmem_row, uint32_t tm_s,
 // Phase dS (needs dP^T): scale*dS^T = P * (dP*scale - D*scale), written as
 // bf16 to TMEM at `pcol` of the dP^T block (the dK product's A operand) and
 // to the swizzled shared tile (row = key r; the dQ product's A operand).
-// `ndsc` holds -D*scale per query.
-template <int D>
+// `ndsc` holds -D*scale per query.  DR: dP of dropped entries is zeroed and
+// `scale` is scale * 256/(256 - t), which gives P * (M dP - D) * scale.
+template <int D, bool DR>
 __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
                                         const float* ndsc, int c0, uint32_t pcol,
                                         int r, float scale,
-                                        const float (&pr)[64]) {
+                                        const float (&pr)[64],
+                                        const uint32_t (&kw)[16]) {
   using C = Cfg<D>;
   uint32_t dr[2][32];
   tmem_ld32(tmem_row + C::TM_DP + 32 * c0, dr[0]);
@@ -189,13 +230,19 @@ __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
     for (int e = 0; e < 32; e += 4) {
       const ulonglong2 dv = d4[(32 * h + e) / 4];
       const float* pe = pr + 32 * h + e;
+      uint32_t g0 = dr[h][e], g1 = dr[h][e + 1], g2 = dr[h][e + 2], g3 = dr[h][e + 3];
+      if constexpr (DR) {
+        const uint32_t w = kw[8 * h + e / 4];
+        g0 &= elem_mask(w, 0);
+        g1 &= elem_mask(w, 1);
+        g2 &= elem_mask(w, 2);
+        g3 &= elem_mask(w, 3);
+      }
       float a0, a1, a2, a3;
-      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(dr[h][e]), __uint_as_float(dr[h][e + 1])),
-                            sc2, dv.x),
+      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(g0), __uint_as_float(g1)), sc2, dv.x),
                       f2_pack(pe[0], pe[1])),
                 a0, a1);
-      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(dr[h][e + 2]), __uint_as_float(dr[h][e + 3])),
-                            sc2, dv.y),
+      f2_unpack(fmul2(ffma2(f2_pack(__uint_as_float(g2), __uint_as_float(g3)), sc2, dv.y),
                       f2_pack(pe[2], pe[3])),
                 a2, a3);
       dd[e / 2] = pack_bf16x2(a0, a1);
@@ -209,10 +256,12 @@ __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
   }
 }
 
-// Reads one 128 x D fp32 accumulator (lanes = rows) and stores row r as bf16.
-template <int D>
+// Reads one 128 x D fp32 accumulator (lanes = rows) and stores row r as bf16
+// (times `mult` when MUL).
+template <int D, bool MUL = false>
 __device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
-                                                __nv_bfloat16* out, bool store) {
+                                                __nv_bfloat16* out, bool store,
+                                                float mult = 1.f) {
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t v[32];
@@ -222,8 +271,14 @@ __device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
     uint4 o[4];
     uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
-      ow[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+    for (int k = 0; k < 16; ++k) {
+      float a = __uint_as_float(v[2 * k]), b = __uint_as_float(v[2 * k + 1]);
+      if constexpr (MUL) {
+        a *= mult;
+        b *= mult;
+      }
+      ow[k] = pack_bf16x2(a, b);
+    }
     if (store) {
       uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
@@ -232,7 +287,7 @@ __device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
   }
 }
 
-template <int D>
+template <int D, bool DR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
@@ -567,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tmem_row = tmem + lane_off;
     const int r = wq * 32 + lane;     // key row (dS, dK, dV) / query row (dQ)
-    const float sl2 = p.scale_log2, scale = p.scale;
+    const float sl2 = p.scale_log2;
+    const float scale = DR ? p.scale * p.drop.keep_scale : p.scale;  // of dP
     uint32_t qcnt = 0, g = 0, it = 0;
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
@@ -580,6 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int iend = sc.q_end(kb);
       for (int i = sc.q_begin(kb); i <= iend; ++i) {
         const int s = qcnt % C::QST;
+        uint32_t kw[16];
+        if constexpr (DR) key_row_keep_words(kw, p.drop, bh, key, i * 128 + 64 * grp, lane);
         if (!wait_warp(bar(C::B_QFULL + s), (qcnt / C::QST) & 1, abort_flag,
                        lim, SITE_S_QFULL) ||
             !wait_warp(bar(C::B_SFULL), g & 1, abort_flag, lim, SITE_S_SFULL)) {
@@ -592,8 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool diag = sc.causal && i == kb;
         const bool edge = sc.window_edge(i, kb);
         float pr[64];
-        p_half(tmem_row, C::TM_S, lse2, 2 * grp, 64u * grp, key, kvalid, diag,
-               sc.window, edge, q0, sl2, pr);
+        p_half<DR>(tmem_row, C::TM_S, lse2, 2 * grp, 64u * grp, key, kvalid, diag,
+                   sc.window, edge, q0, sl2, pr, kw);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(C::B_PREADY));
@@ -602,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        ds_half<D>(tmem_row, smem, lse2 + 128, 2 * grp, 64u * grp, r, scale, pr);
+        ds_half<D, DR>(tmem_row, smem, lse2 + 128, 2 * grp, 64u * grp, r, scale, pr, kw);
         tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
@@ -649,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool store = key < N;
       const size_t rowoff = ((size_t)bh * N + (size_t)(store ? key : 0)) * D;
       if (grp == 0)
-        store_rows_bf16<D>(tmem_row + C::TM_DV, p.dV + rowoff, store);
+        store_rows_bf16<D, DR>(tmem_row + C::TM_DV, p.dV + rowoff, store,
+                               p.drop.keep_scale);
       else
         store_rows_bf16<D>(tmem_row + C::TM_DK, p.dK + rowoff, store);
       tc_fence_before();
@@ -664,13 +723,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D>
+template <int D, bool DR>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
                    const float* Dvec, void* dK, void* dV, int num_sms,
                    uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D>;
   static cudaError_t attr = cudaFuncSetAttribute(
-      bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      bwd_kernel<D, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   Params p;
   p.LSE = LSE;
@@ -680,12 +739,13 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   p.scale = s.scale;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.wait_limit_ns = lim;
+  p.drop = s.drop;
   const int BH = s.B * s.H;
   const int n_blk = (s.N + 127) / 128;
   const int total = BH * n_blk;
   const int grid = total < num_sms ? total : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  bwd_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
+  bwd_kernel<D, DR><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, p);
   return cudaGetLastError();
 }
@@ -697,11 +757,13 @@ cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
                           void* dK, void* dV, int num_sms,
                           uint64_t wait_limit_ns, cudaStream_t stream) {
   (void)dQacc;  // reached through maps.dq_acc
+  const bool dr = s.drop.t4 != 0;
+  const uint64_t lim = wait_limit_ns;
   if (s.d == 64)
-    return bwdtc::launch<64>(s, maps, LSE, Dvec, dK, dV, num_sms, wait_limit_ns,
-                             stream);
-  return bwdtc::launch<128>(s, maps, LSE, Dvec, dK, dV, num_sms, wait_limit_ns,
-                            stream);
+    return dr ? bwdtc::launch<64, true>(s, maps, LSE, Dvec, dK, dV, num_sms, lim, stream)
+              : bwdtc::launch<64, false>(s, maps, LSE, Dvec, dK, dV, num_sms, lim, stream);
+  return dr ? bwdtc::launch<128, true>(s, maps, LSE, Dvec, dK, dV, num_sms, lim, stream)
+            : bwdtc::launch<128, false>(s, maps, LSE, Dvec, dK, dV, num_sms, lim, stream);
 }
 
 FA_DEFINE_STATUS_READER(read_status_bwd_tc)

@@ -26,9 +26,17 @@
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d); P_t aliases the first 64 columns of
 // S_t as packed bf16 pairs.
+//
+// With dropout (the DR variant), each softmax thread also draws the keep
+// bytes of its row: per 32-key quarter of a block, two Philox calls per lane
+// give the quad's four rows x 32 keys, a quad transpose hands every lane its
+// own row's words, and P is written to TMEM with the dropped entries zeroed.
+// The row sum l stays that of the undropped row (so LSE is unchanged) and
+// the factor 256/(256 - t) of kept entries is folded into the final 1/l.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "fa_sched.cuh"
 #include "fa_tiles.cuh"
 
@@ -74,6 +82,7 @@ struct Params {
   float* LSE;
   float scale_log2;  // scale * log2(e)
   uint64_t wait_limit_ns;
+  DropSpec drop;     // used by the DR variant only
   FwdSched sched;
 };
 
@@ -84,9 +93,9 @@ enum : uint32_t {
   SITE_ALIGN
 };
 
-// W: the causal sliding-window variant (compiled separately, so that the
-// plain kernels carry none of its range bookkeeping).
-template <int D, bool W>
+// W: the causal sliding-window variant, DR: dropout (each compiled
+// separately, so that the plain kernels carry none of their bookkeeping).
+template <int D, bool W, bool DR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
@@ -431,6 +440,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tO + 0, oa[0]);
             tmem_ld32(tO + 32, oa[1]);
           }
+          // keep bytes of this row for keys 32h + 4c + (0..3), c = 0..7: lane
+          // q of the quad draws key patches q and 4 + q for the quad's four
+          // rows (word = row mod 4), the transpose collects this row's words
+          uint32_t kw[8];
+          if constexpr (DR) {
+            const uint32_t kp0 = (uint32_t)(j * 32 + 8 * h) + (uint32_t)(lane & 3);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const Philox4 o = philox4x32_10(kp0 + 4 * g, (uint32_t)row >> 2,
+                                              (uint32_t)bh, 0u, p.drop.k0, p.drop.k1);
+              uint32_t a[4] = {o.x[0], o.x[1], o.x[2], o.x[3]};
+              quad_transpose(a, lane);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_bytes(a[c], p.drop.t4);
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -441,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             b = ex2_approx(b);
             acc[i & 3] = fadd2(acc[i & 3], f2_pack(a, b));
             pk[i] = pack_bf16x2(a, b);
+            if constexpr (DR) pk[i] &= pair_mask(kw[i >> 1], i);
           }
           tmem_st16(tS + 16 * h, pk);
         }
@@ -496,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       ++ocnt;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      // kept entries carry the factor 256/(256 - t)
+      const float inv_l = (DR ? p.drop.keep_scale : 1.f) / l;
       const bool store = row < sc.N;
       __nv_bfloat16* orow = p.O + ((size_t)bh * sc.N + (size_t)(store ? row : 0)) * D;
 #pragma unroll
@@ -531,14 +558,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool W>
+template <int D, bool W, bool DR>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
                    float* LSE, int num_sms, uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D>;
   static bool attr_done = false;  // per process; same value on every device
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(
-        fwd_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        fwd_kernel<D, W, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -548,13 +575,14 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   p.LSE = LSE;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.wait_limit_ns = lim;
+  p.drop = s.drop;
   const int BH = s.B * s.H;
   FwdSched probe;
   probe.init(BH, s.N, s.causal, num_sms, s.window);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  fwd_kernel<D, W><<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps.q, maps.k,
-                                                                maps.v, p);
+  fwd_kernel<D, W, DR><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
+      maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
@@ -563,12 +591,18 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
 cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
                           float* LSE, int num_sms, uint64_t wait_limit_ns,
                           cudaStream_t stream) {
-  const bool w = s.window > 0;
-  if (s.d == 64)
-    return w ? fwdtc::launch<64, true>(s, maps, O, LSE, num_sms, wait_limit_ns, stream)
-             : fwdtc::launch<64, false>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
-  return w ? fwdtc::launch<128, true>(s, maps, O, LSE, num_sms, wait_limit_ns, stream)
-           : fwdtc::launch<128, false>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+  const int v = (s.window > 0 ? 1 : 0) + (s.drop.t4 != 0 ? 2 : 0);
+  const uint64_t lim = wait_limit_ns;
+#define FA_FWD_CASE(DD)                                                        \
+  switch (v) {                                                                 \
+    case 0: return fwdtc::launch<DD, false, false>(s, maps, O, LSE, num_sms, lim, stream); \
+    case 1: return fwdtc::launch<DD, true, false>(s, maps, O, LSE, num_sms, lim, stream);  \
+    case 2: return fwdtc::launch<DD, false, true>(s, maps, O, LSE, num_sms, lim, stream);  \
+    default: return fwdtc::launch<DD, true, true>(s, maps, O, LSE, num_sms, lim, stream);  \
+  }
+  if (s.d == 64) FA_FWD_CASE(64)
+  FA_FWD_CASE(128)
+#undef FA_FWD_CASE
 }
 
 FA_DEFINE_STATUS_READER(read_status_fwd_tc)

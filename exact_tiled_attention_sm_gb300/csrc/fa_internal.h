@@ -7,11 +7,22 @@
 
 namespace fa {
 
+// Dropout parameters as the kernels take them: the byte threshold t (keep
+// iff the random byte is >= t) in all four bytes, t4 = 0 meaning no dropout;
+// the factor 256/(256 - t) of a kept entry; the Philox key (seed low word,
+// seed high word).
+struct DropSpec {
+  uint32_t t4 = 0;
+  float keep_scale = 1.f;
+  uint32_t k0 = 0, k1 = 0;
+};
+
 struct AttnShape {
   int B, H, N, d;
   float scale;
   int causal;
   int window = 0;  // > 0: causal sliding window of this many keys
+  DropSpec drop{};
 };
 
 // TMA descriptors (built by fa_api.cu): the bf16 [B*H, N, d] tensors with
@@ -48,6 +59,9 @@ cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
 cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
                            int is_bf16, float* Dvec, float* dQacc,
                            cudaStream_t stream);
+// keep[bh][r][k] = 1 if dropout keeps (r, k), else 0 (bytes, B*H*N*N).
+cudaError_t launch_dropout_mask(const AttnShape& s, uint8_t* keep,
+                                cudaStream_t stream);
 // dQ (bf16) = dQacc.
 cudaError_t launch_dq_convert(const AttnShape& s, const float* dQacc, void* dQ,
                               cudaStream_t stream);

@@ -8,9 +8,13 @@
 // warps owns 32 query rows; for every key block each warp takes 8 rows, lane
 // k scores key k, and the row max and row sum are warp-shuffle reductions.
 // Causal key blocks after the query block are skipped.
+//
+// Dropout in the fp32 kernels: each thread holds single (query, key) entries
+// and draws each one's keep decision with its own Philox call (keep_one).
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "fa_philox.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -47,7 +51,7 @@ __global__ void __launch_bounds__(128)
     fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                    const float* __restrict__ V, float* __restrict__ O,
                    float* __restrict__ LSE, int N, float scale, int causal,
-                   int window) {
+                   int window, const DropSpec drop) {
   constexpr int LD = D + 1;  // padded: lane k reads row k without conflicts
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][D]
@@ -88,14 +92,15 @@ __global__ void __launch_bounds__(128)
       const float m_new = fmaxf(m[rr], warp_max(s));
       const float corr = (m_new == -INFINITY) ? 1.f : expf(m[rr] - m_new);
       const float pr = (s == -INFINITY) ? 0.f : expf(s - m_new);
-      l[rr] = l[rr] * corr + warp_sum(pr);
+      l[rr] = l[rr] * corr + warp_sum(pr);  // the undropped row sum
       m[rr] = m_new;
+      const float pv = (drop.t4 == 0 || keep_one(drop, bh, row, key)) ? pr : 0.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float acc = 0.f;
 #pragma unroll 8
         for (int k = 0; k < kKeys; ++k)
-          acc = fmaf(__shfl_sync(0xffffffffu, pr, k), sV[k * D + c * 32 + lane], acc);
+          acc = fmaf(__shfl_sync(0xffffffffu, pv, k), sV[k * D + c * 32 + lane], acc);
         o[rr][c] = o[rr][c] * corr + acc;
       }
     }
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(128)
   for (int rr = 0; rr < 8; ++rr) {
     const int row = r0 + warp * 8 + rr;
     if (row >= N) continue;
-    const float inv = 1.f / l[rr];
+    const float inv = drop.keep_scale / l[rr];
 #pragma unroll
     for (int c = 0; c < D / 32; ++c)
       O[head + (size_t)row * D + c * 32 + lane] = o[rr][c] * inv;
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(128)
                         const float* __restrict__ V, const float* __restrict__ dO,
                         const float* __restrict__ LSE, const float* __restrict__ Dv,
                         float* __restrict__ dK, float* __restrict__ dV, int N,
-                        float scale, int causal, int window) {
+                        float scale, int causal, int window, const DropSpec drop) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][LD]
@@ -163,13 +168,16 @@ __global__ void __launch_bounds__(128)
       const bool vis = qvalid && key < N && !(causal && key > qrow) &&
                        !(window > 0 && qrow - key >= window);
       const float pr = vis ? expf(s * scale - lse) : 0.f;
-      const float ds = pr * (dp - Dq);
+      // dropout: P o M for dV (the factor applied at the end), P (M dP - D)
+      const bool kept = drop.t4 == 0 || keep_one(drop, bh, qrow, key);
+      const float pv = kept ? pr : 0.f;
+      const float ds = pr * ((kept ? dp * drop.keep_scale : 0.f) - Dq);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float a1 = 0.f, a2 = 0.f;
 #pragma unroll 8
         for (int q = 0; q < kRows; ++q) {
-          a1 = fmaf(__shfl_sync(0xffffffffu, pr, q), sdO[q * LD + c * 32 + lane], a1);
+          a1 = fmaf(__shfl_sync(0xffffffffu, pv, q), sdO[q * LD + c * 32 + lane], a1);
           a2 = fmaf(__shfl_sync(0xffffffffu, ds, q), sQ[q * LD + c * 32 + lane], a2);
         }
         av[i][c] += a1;
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(128)
     if (key >= N) continue;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      dV[head + (size_t)key * D + c * 32 + lane] = av[i][c];
+      dV[head + (size_t)key * D + c * 32 + lane] = av[i][c] * drop.keep_scale;
       dK[head + (size_t)key * D + c * 32 + lane] = ak[i][c] * scale;
     }
   }
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(128)
                       const float* __restrict__ V, const float* __restrict__ dO,
                       const float* __restrict__ LSE, const float* __restrict__ Dv,
                       float* __restrict__ dQ, int N, float scale, int causal,
-                      int window) {
+                      int window, const DropSpec drop) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][D]
@@ -238,7 +246,8 @@ __global__ void __launch_bounds__(128)
       const bool vis = rvalid && key < N && !(causal && key > row) &&
                        !(window > 0 && row - key >= window);
       const float pr = vis ? expf(s * scale - lse) : 0.f;
-      const float ds = pr * (dp - Dq);
+      const bool kept = drop.t4 == 0 || keep_one(drop, bh, row, key);
+      const float ds = pr * ((kept ? dp * drop.keep_scale : 0.f) - Dq);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         float a = 0.f;
@@ -278,6 +287,31 @@ __global__ void __launch_bounds__(256)
   if (dQacc) {
 #pragma unroll
     for (int c = lane; c < D; c += 32) dQacc[row * D + c] = 0.f;
+  }
+}
+
+// keep[bh][r][k] = 1 when dropout keeps (r, k), else 0: one thread per 4 x 4
+// patch (one Philox call), patches of one row of patches along x, heads
+// along z.
+__global__ void __launch_bounds__(128)
+    dropout_mask_kernel(uint8_t* __restrict__ keep, int BH, int N, const DropSpec d) {
+  const int np = (N + 3) / 4;
+  const int kp = blockIdx.x * blockDim.x + threadIdx.x;
+  const int rp = blockIdx.y;
+  if (kp >= np) return;
+  for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
+    const Philox4 o = philox4x32_10((uint32_t)kp, (uint32_t)rp, (uint32_t)bh, 0u,
+                                    d.k0, d.k1);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int r = 4 * rp + w;
+      if (r >= N) break;
+      const uint32_t kb = keep_bytes(o.x[w], d.t4) & 0x01010101u;
+      uint8_t* dst = keep + ((size_t)bh * N + r) * N + 4 * (size_t)kp;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (4 * kp + b < N) dst[b] = (uint8_t)((kb >> (8 * b)) & 1u);
+    }
   }
 }
 
@@ -327,8 +361,8 @@ static cudaError_t fwd_f32_launch(const AttnShape& s, const float* Q,
   static cudaError_t attr = smem_attr(simt::fwd_f32_kernel<D>, bytes);
   if (attr != cudaSuccess) return attr;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
-  simt::fwd_f32_kernel<D><<<grid, 128, bytes, stream>>>(Q, K, V, O, LSE, s.N,
-                                                        s.scale, s.causal, s.window);
+  simt::fwd_f32_kernel<D><<<grid, 128, bytes, stream>>>(
+      Q, K, V, O, LSE, s.N, s.scale, s.causal, s.window, s.drop);
   return cudaGetLastError();
 }
 
@@ -345,11 +379,11 @@ static cudaError_t bwd_f32_launch(const AttnShape& s, const float* Q,
   if (a2 != cudaSuccess) return a2;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
   simt::bwd_f32_dkdv_kernel<D><<<grid, 128, bytes, stream>>>(
-      Q, K, V, dO, LSE, Dvec, dK, dV, s.N, s.scale, s.causal, s.window);
+      Q, K, V, dO, LSE, Dvec, dK, dV, s.N, s.scale, s.causal, s.window, s.drop);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   simt::bwd_f32_dq_kernel<D><<<grid, 128, bytes, stream>>>(
-      Q, K, V, dO, LSE, Dvec, dQ, s.N, s.scale, s.causal, s.window);
+      Q, K, V, dO, LSE, Dvec, dQ, s.N, s.scale, s.causal, s.window, s.drop);
   return cudaGetLastError();
 }
 
@@ -389,6 +423,16 @@ cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
     else
       simt::bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_mask(const AttnShape& s, uint8_t* keep,
+                                cudaStream_t stream) {
+  const int np = (s.N + 3) / 4;
+  const int BH = s.B * s.H;
+  dim3 grid((unsigned)((np + 127) / 128), (unsigned)np,
+            (unsigned)(BH < 65535 ? BH : 65535));
+  simt::dropout_mask_kernel<<<grid, 128, 0, stream>>>(keep, BH, s.N, s.drop);
   return cudaGetLastError();
 }
 

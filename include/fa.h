@@ -102,6 +102,53 @@ fa_status fa_bwd_window(const void* Q, const void* K, const void* V,
                         int d, float scale, int window, fa_dtype dt,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* Attention dropout ("Flash Attention, From First Principles", "Honesty
+ * time -- the confession list", item 4: the extra lines of the paper's
+ * algorithm 2), forward and backward.  After the softmax each probability
+ * p_rk is multiplied by M_rk = keep_rk * 256 / (256 - t), keep_rk in {0, 1},
+ * so O = (P o M) V; LSE is that of the undropped row.  The backward uses
+ * dV = (P o M)^T dO, dS = P o (M o dP - D) with D = rowsum(dO * O).
+ *   - t = round(256 * dropout_p), ties to even (fa_dropout_threshold); each
+ *     entry is dropped with probability t/256.  dropout_p must be finite and
+ *     round to t <= 255; t = 0 is the computation without dropout.
+ *   - keep_rk comes from Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ *     random numbers: as easy as 1, 2, 3", SC'11) with key (seed & 0xFFFFFFFF,
+ *     seed >> 32) and counter (k/4, r/4, b*H + h, 0): byte (k mod 4) of output
+ *     word (r mod 4) is (r, k)'s, and keep_rk = (byte >= t).  The mask is a
+ *     pure function of (seed, head, r, k): no state is kept between calls,
+ *     and fa_bwd_dropout with the forward's seed regenerates the forward's
+ *     mask exactly.
+ *   - causal and window select the mask as in fa_fwd / fa_fwd_window: window
+ *     = 0 means none (causal decides), window >= 1 a causal sliding window.
+ * The other arguments and conventions are those of fa_fwd / fa_bwd.
+ * Errors: as fa_fwd / fa_bwd, plus FA_ERR_INVALID_ARG for window < 0 or a
+ * dropout_p outside the range above. */
+fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V, void* O,
+                         float* LSE, int B, int H, int N, int d, float scale,
+                         int causal, int window, float dropout_p,
+                         unsigned long long seed, fa_dtype dt, void* stream);
+fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V,
+                         const void* O, const void* dO, const float* LSE,
+                         void* dQ, void* dK, void* dV, int B, int H, int N,
+                         int d, float scale, int causal, int window,
+                         float dropout_p, unsigned long long seed, fa_dtype dt,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The byte threshold t of a dropout probability (see fa_fwd_dropout), or -1
+ * when fa_fwd_dropout would reject it.  Pure host arithmetic. */
+int fa_dropout_threshold(float dropout_p);
+
+/* Writes the keep mask of fa_fwd_dropout to `keep`: caller-owned device
+ * memory of B*H*N*N bytes in [B][H][r][k] order, 1 where (r, k) is kept and
+ * 0 where it is dropped (for every pair, whatever the causal or window
+ * mask).  For inspection and testing; the attention entry points never
+ * store the mask.  Asynchronous on `stream`.
+ * Errors: FA_ERR_INVALID_ARG for a null pointer, B, H or N < 1, N > 262140,
+ * or a dropout_p fa_dropout_threshold rejects; FA_ERR_CUDA. */
+fa_status fa_dropout_mask(unsigned char* keep, int B, int H, int N,
+                          float dropout_p, unsigned long long seed,
+                          void* stream);
+
 /* Size of the device scratch array that fa_bwd_noalloc uses in place of a
  * caller workspace: 64 MiB, statically reserved on every GPU that loads the
  * library (the reservation lasts until the process exits). */

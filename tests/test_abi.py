@@ -138,6 +138,35 @@ def test_window_entry_points_reject_bad_windows(L):
         fa.fa_fwd_schedule_census_window(16, 1, -1)
 
 
+def test_dropout_threshold_matches_the_oracle(L):
+    """t = round(256 p) with ties to even, on both sides; values exact in fp32
+    so that both sides round the same number."""
+    import numpy as np
+    ps = [0.0, 0.1, 0.25, 0.5, 0.9, 1 / 512, 3 / 512, 5 / 512, 509 / 512,
+          510.9 / 512, 0.3333]
+    for p in ps:
+        p32 = float(np.float32(p))
+        assert fa.fa_dropout_threshold(p32) == oracle.dropout_threshold(p32), p
+    for p in (-1e-9, -0.5, 511 / 512, 1.0, 2.0, float("nan"), float("inf")):
+        assert fa.fa_dropout_threshold(p) == -1, p
+
+
+def test_dropout_entry_points_reject_bad_arguments(L):
+    a = [16, 16, 16, 16, 16, 1, 1, 16, 64, 0.1]
+    n = fa.fa_bwd_workspace_size(1, 1, 16, 64)
+    b = [256] * 9 + [1, 1, 16, 64, 0.1]
+    for causal, window, p in ((0, 0, -0.1), (0, 0, 1.0), (1, -1, 0.1),
+                              (0, 0, float("nan"))):
+        assert fa.fa_fwd_dropout(*a, causal, window, p, 1, fa.FA_BF16,
+                                 None) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_bwd_dropout(*b, causal, window, p, 1, fa.FA_BF16, 256, n,
+                                 None) == fa.FA_ERR_INVALID_ARG
+    for args in ((None, 1, 1, 16, 0.1, 0), (16, 0, 1, 16, 0.1, 0),
+                 (16, 1, 1, 0, 0.1, 0), (16, 1, 1, 300000, 0.1, 0),
+                 (16, 1, 1, 16, 1.5, 0)):
+        assert fa.fa_dropout_mask(*args, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_library_has_no_oracle_symbols(L):
     """The product library and the oracle share nothing."""
     assert not hasattr(L, "oracle_fwd")

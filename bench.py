@@ -183,7 +183,8 @@ def max_over_ranks(x, world):
 def run_profile(args):
     """Only the launches of one workload (for ncu): W warm-up steps then K
     steps, nothing else on the GPU.  `train_fwd_bwd` runs fa_fwd + fa_bwd
-    (4 launches a step); a forward workload runs fa_fwd (1 launch a step)."""
+    (4 launches a step); a forward workload runs fa_fwd (1 launch a step).
+    --window and --dropout select those variants."""
     import torch
     import exact_tiled_attention_sm_gb300 as fa
     from exact_tiled_attention_sm_gb300 import inputs
@@ -198,16 +199,18 @@ def run_profile(args):
         do = x["dO"].cuda()
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = fa.workspace(w.B, w.H, w.N, w.d)
+    opt = {"window": args.window, "dropout_p": args.dropout, "seed": 1234}
     for _ in range(args.warmup + args.steps):
-        fa.fwd(q, k, v, w.scale, causal, out=o, lse=lse)
+        fa.fwd(q, k, v, w.scale, causal, out=o, lse=lse, **opt)
         if w.passes == "fwd+bwd":
-            fa.bwd(q, k, v, o, do, lse, w.scale, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+            fa.bwd(q, k, v, o, do, lse, w.scale, causal, dq=dq, dk=dk, dv=dv, ws=ws,
+                   **opt)
     torch.cuda.synchronize()
     st = fa.last_device_status()
     if st != fa.FA_OK:
         raise SystemExit(f"device status: {fa.status_string(st)}")
     return {"profile": args.workload, "causal": causal, "steps": args.steps,
-            "warmup": args.warmup}
+            "warmup": args.warmup, "window": args.window, "dropout": args.dropout}
 
 
 # --------------------------------------------------------------------- ours
@@ -352,11 +355,9 @@ def run_ours(args):
             launches += reps
         del qf, kf, vf, of, lf
 
-    # --- causal sliding window ("LLM Architecture Refresh [3]", section 5):
-    # a long-context forward with a 4096-key window, and the training step's
-    # shape with a 512-key window (fwd + bwd); FLOPs over the visible pairs
-    window_results = {}
-    for name, win, passes in (("long_ctx_32k", 4096, "fwd"), (WORKLOAD, 512, "fwd+bwd")):
+    def time_variant(name, passes, causal_v, win=0, drop=0.0, seed=0):
+        """Device time of one fa_fwd (+ fa_bwd) call pair of a mask or dropout
+        variant on workload `name`; returns (ms per call pair, launches timed)."""
         wf = inputs.WORKLOADS[name]
         xf = inputs.workload_inputs(wf, with_dO=(passes != "fwd"))
         qf, kf, vf = (xf[n].cuda() for n in ("Q", "K", "V"))
@@ -367,30 +368,52 @@ def run_ours(args):
             dqf, dkf, dvf = torch.empty_like(qf), torch.empty_like(qf), torch.empty_like(qf)
             wsf = fa.workspace(wf.B, wf.H, wf.N, wf.d)
 
-        def wstep():
-            fa.fwd(qf, kf, vf, wf.scale, True, out=of, lse=lf, window=win)
+        def vstep():
+            fa.fwd(qf, kf, vf, wf.scale, causal_v, out=of, lse=lf, window=win,
+                   dropout_p=drop, seed=seed)
             if passes != "fwd":
-                fa.bwd(qf, kf, vf, of, dof, lf, wf.scale, True, dq=dqf, dk=dkf,
-                       dv=dvf, ws=wsf, window=win)
+                fa.bwd(qf, kf, vf, of, dof, lf, wf.scale, causal_v, dq=dqf, dk=dkf,
+                       dv=dvf, ws=wsf, window=win, dropout_p=drop, seed=seed)
 
         reps = max(5, args.steps // 4)
         for _ in range(3):
-            wstep()
+            vstep()
         barrier(world)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(reps):
-            wstep()
+            vstep()
         b.record(stream)
         barrier(world)
         ms = max_over_ranks(a.elapsed_time(b), world) / reps
+        return ms, reps * (1 if passes == "fwd" else 4)
+
+    # --- causal sliding window ("LLM Architecture Refresh [3]", section 5):
+    # a long-context forward with a 4096-key window, and the training step's
+    # shape with a 512-key window (fwd + bwd); FLOPs over the visible pairs
+    window_results = {}
+    for name, win, passes in (("long_ctx_32k", 4096, "fwd"), (WORKLOAD, 512, "fwd+bwd")):
+        wf = inputs.WORKLOADS[name]
+        ms, nl = time_variant(name, passes, True, win=win)
         fl = window_flops(wf.B, wf.H, wf.N, wf.d, win, passes)
         window_results[f"{name}_w{win}_{passes.replace('+', '_')}"] = {
             "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
-            "window": win, "launches": reps * (1 if passes == "fwd" else 4)}
-        launches += reps * (1 if passes == "fwd" else 4)
-        del qf, kf, vf, of, lf
+            "window": win, "launches": nl}
+        launches += nl
+
+    # --- attention dropout (p = 0.1; the backward regenerates the keep mask
+    # from the seed): the 4096-token forward without a mask and the training
+    # step; FLOPs those of the same computation without dropout
+    dropout_results = {}
+    for name, causal_v, passes in (("llama3_8b_fwd", False, "fwd"), (WORKLOAD, True, "fwd+bwd")):
+        wf = inputs.WORKLOADS[name]
+        ms, nl = time_variant(name, passes, causal_v, drop=0.1, seed=1234)
+        fl = attn_flops(wf.B, wf.H, wf.N, wf.d, causal_v, passes)
+        dropout_results[f"{name}{'_causal' if causal_v else ''}_p0.1_{passes.replace('+', '_')}"] = {
+            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "dropout_p": 0.1, "launches": nl}
+        launches += nl
     clocks = sampler.stop()
     st = fa.last_device_status()
     if st != fa.FA_OK:
@@ -405,7 +428,8 @@ def run_ours(args):
     bwd_flops = step_flops - attn_flops(B, H, N, d, causal, "fwd")
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = attn_flops(B, H, N, d, causal, "fwd") / (fwd_ms * 1e-3) / 1e12
-    for r in list(fwd_results.values()) + list(window_results.values()):
+    for r in (list(fwd_results.values()) + list(window_results.values())
+              + list(dropout_results.values())):
         r["frac_of_peak"] = round(r["tflops"] / world / peak, 4)
     line = {
         "metric": METRIC,
@@ -448,6 +472,7 @@ def run_ours(args):
         },
         "fwd": fwd_results,
         "window": window_results,
+        "dropout": dropout_results,
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -539,6 +564,8 @@ def main():
                     help="run only --workload's launches (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--causal", type=int, default=1)
+    ap.add_argument("--window", type=int, default=0, help="profile: sliding window")
+    ap.add_argument("--dropout", type=float, default=0.0, help="profile: dropout p")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.profile:

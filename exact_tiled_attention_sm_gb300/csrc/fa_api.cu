@@ -134,6 +134,8 @@ fa::DropSpec drop_spec(int t, unsigned long long seed) {
   if (t > 0) {
     d.t4 = (uint32_t)t * 0x01010101u;
     d.keep_scale = (float)(256.0 / (double)(256 - t));
+    d.c4 = (uint32_t)(256 - t) * 0x01010101u;
+    d.c7 = d.c4 & 0x7F7F7F7Fu;
   }
   d.k0 = (uint32_t)seed;
   d.k1 = (uint32_t)(seed >> 32);

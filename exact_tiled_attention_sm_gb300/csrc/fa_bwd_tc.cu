@@ -113,8 +113,8 @@ enum : uint32_t {
 };
 
 // Keep words of key row `key` for the 64 queries q_base + (0..63): word c
-// holds the keep bytes (0xFF kept, 0x00 dropped) of queries q_base + 4c +
-// (0..3).  Lane q of a quad (keys 4*(key/4) + 0..3) draws the query patches
+// holds the keep flags (keep_flags: top bit of each byte) of queries
+// q_base + 4c + (0..3).  Lane q of a quad (keys 4*(key/4) + 0..3) draws the query patches
 // 4g + q, g = 0..3; each call's words are indexed by query, its bytes by key,
 // so a byte transpose regroups them by key and a quad transpose hands each
 // lane its own key's words.
@@ -130,7 +130,7 @@ __device__ __forceinline__ void key_row_keep_words(uint32_t (&kw)[16],
     byte_transpose(a);
     quad_transpose(a, lane);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_bytes(a[c], d.t4);
+    for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_flags(a[c], d);
   }
 }
 

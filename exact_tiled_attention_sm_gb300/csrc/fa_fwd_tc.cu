@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t a[4] = {o.x[0], o.x[1], o.x[2], o.x[3]};
               quad_transpose(a, lane);
 #pragma unroll
-              for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_bytes(a[c], p.drop.t4);
+              for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_flags(a[c], p.drop);
             }
           }
           uint32_t pk[16];

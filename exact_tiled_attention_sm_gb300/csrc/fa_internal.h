@@ -10,11 +10,13 @@ namespace fa {
 // Dropout parameters as the kernels take them: the byte threshold t (keep
 // iff the random byte is >= t) in all four bytes, t4 = 0 meaning no dropout;
 // the factor 256/(256 - t) of a kept entry; the Philox key (seed low word,
-// seed high word).
+// seed high word); and 256 - t in all four bytes, whole (c4) and without
+// each byte's top bit (c7), for the carry-based byte compare (t >= 1).
 struct DropSpec {
   uint32_t t4 = 0;
   float keep_scale = 1.f;
   uint32_t k0 = 0, k1 = 0;
+  uint32_t c4 = 0, c7 = 0;
 };
 
 struct AttnShape {

@@ -54,9 +54,19 @@ __host__ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t 
   return Philox4{{x0, x1, x2, x3}};
 }
 
-// 0xFF in every byte of w that is >= t, 0x00 in the others.
+// 0xFF in every byte of w that is >= t, 0x00 in the others (any t).
 __device__ __forceinline__ uint32_t keep_bytes(uint32_t w, uint32_t t4) {
   return __vcmpgeu4(w, t4);
+}
+
+// The same decisions in three operations, for t >= 1: bit 7 of byte j of the
+// result is set iff byte j of w is >= t, i.e. iff w_j + (256 - t) carries out
+// of the byte.  s holds the sums of the low seven bits, so its bit 7 is the
+// carry into bit 7; the carry out is the majority of that carry and the two
+// top bits.  The other bits of the result are meaningless.
+__device__ __forceinline__ uint32_t keep_flags(uint32_t w, const DropSpec& d) {
+  const uint32_t s = (w & 0x7F7F7F7Fu) + d.c7;
+  return (w & d.c4) | ((w | d.c4) & s);
 }
 
 // Byte selection: four bytes taken from the pair (a, b) by the 16-bit selector
@@ -101,14 +111,15 @@ __device__ __forceinline__ void byte_transpose(uint32_t (&w)[4]) {
 }
 
 // Keep mask (0xFFFF per kept element) of the bf16 pair at elements 2i, 2i+1
-// of a keep word (elements 0-3 = its bytes).
-__device__ __forceinline__ uint32_t pair_mask(uint32_t kw, int i) {
-  return byte_perm(kw, 0u, (i & 1) ? 0x3322u : 0x1100u);
+// of a keep_flags word (elements 0-3 = its bytes): selector nibbles 8-15 copy
+// the top bit of a byte into all eight bits.
+__device__ __forceinline__ uint32_t pair_mask(uint32_t kf, int i) {
+  return byte_perm(kf, 0u, (i & 1) ? 0xBBAAu : 0x9988u);
 }
 
-// Keep mask (all ones when kept) of element e (0..3) of a keep word.
-__device__ __forceinline__ uint32_t elem_mask(uint32_t kw, int e) {
-  return byte_perm(kw, 0u, 0x1111u * (uint32_t)e);
+// Keep mask (all ones when kept) of element e (0..3) of a keep_flags word.
+__device__ __forceinline__ uint32_t elem_mask(uint32_t kf, int e) {
+  return byte_perm(kf, 0u, 0x8888u | (0x1111u * (uint32_t)e));
 }
 
 // The decision for one (head bh, query r, key k), one Philox call per entry

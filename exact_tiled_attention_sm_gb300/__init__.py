@@ -18,7 +18,7 @@ FA_BF16, FA_F32 = 0, 1
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_fwd_window",
-           "fa_bwd_window", "fa_fwd_dropout", "fa_bwd_dropout",
+           "fa_bwd_window", "fa_fwd_dropout", "fa_bwd_dropout", "fa_fwd_fp8",
            "fa_dropout_threshold", "fa_dropout_mask", "fa_bwd_noalloc",
            "fa_last_device_status",
            "fa_status_string", "fa_selftest_wait_timeout",
@@ -64,6 +64,9 @@ def lib():
                                      i, i, f, i, i, f, u64, i, vp,
                                      ctypes.c_size_t, vp]
         L.fa_bwd_dropout.restype = i
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, f, f,
+                                 f, vp]
+        L.fa_fwd_fp8.restype = i
         L.fa_dropout_threshold.argtypes = [f]
         L.fa_dropout_threshold.restype = i
         L.fa_dropout_mask.argtypes = [vp, i, i, i, f, u64, vp]
@@ -129,6 +132,13 @@ def fa_bwd_dropout(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, scale, causal,
                                 scale, int(causal), int(window),
                                 float(dropout_p), int(seed), dt, workspace,
                                 workspace_bytes, stream)
+
+
+def fa_fwd_fp8(Q, K, V, O, LSE, B, H, N, d, scale, causal, window, q_descale,
+               k_descale, v_descale, stream):
+    return lib().fa_fwd_fp8(Q, K, V, O, LSE, B, H, N, d, scale, int(causal),
+                            int(window), float(q_descale), float(k_descale),
+                            float(v_descale), stream)
 
 
 def fa_dropout_threshold(dropout_p):
@@ -244,6 +254,34 @@ def fwd(q, k, v, scale, causal=False, out=None, lse=None, stream=None,
     if st != FA_OK:
         raise FAError(st, "fa_fwd_dropout" if dropout_p else
                       "fa_fwd_window" if window else "fa_fwd")
+    return out, lse
+
+
+def fwd_fp8(q8, k8, v8, scale, descales, causal=False, out=None, lse=None,
+            stream=None, window=0):
+    """O (bf16), LSE = attention forward of E4M3 [B, H, N, 128] CUDA tensors
+    (torch.float8_e4m3fn or their raw uint8 bytes) standing for
+    descales[0] * q8, descales[1] * k8, descales[2] * v8 (fa_fwd_fp8)."""
+    import torch
+    B, H, N, d = q8.shape
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _check_tensor(t, (B, H, N, d), n)
+        if t.element_size() != 1:
+            raise TypeError(f"{n} must hold one byte per element (E4M3)")
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    _check_tensor(out, (B, H, N, d), "out")
+    _check_tensor(lse, (B, H, N), "lse")
+    if out.dtype != torch.bfloat16:
+        raise TypeError("out must be bf16")
+    qd, kd, vd = descales
+    st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                    lse.data_ptr(), B, H, N, d, float(scale), causal, window,
+                    qd, kd, vd, _stream_ptr(stream))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_fp8")
     return out, lse
 
 

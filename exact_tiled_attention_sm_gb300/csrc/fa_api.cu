@@ -84,6 +84,22 @@ fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// [B*H, N, d] 8-bit tensor; boxes of 128 columns (bytes) x 128 rows x 1
+// head, 128-byte swizzle, out-of-range rows read as zero.
+fa_status make_map_u8(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)N * d};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 // fp32 [B*H, N, d] dQ accumulator; boxes of 32 columns x 128 rows x 1 head,
 // 128-byte swizzle; used only as the target of bulk reduce-adds.
 fa_status make_map_f32(CUtensorMap* m, const void* base, int BH, int N, int d) {
@@ -195,6 +211,42 @@ FA_API fa_status fa_fwd_window(const void* Q, const void* K, const void* V,
 }
 
 FA_API int fa_dropout_threshold(float dropout_p) { return threshold_of(dropout_p); }
+
+FA_API fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V,
+                            void* O, float* LSE, int B, int H, int N, int d,
+                            float scale, int causal, int window,
+                            float q_descale, float k_descale, float v_descale,
+                            void* stream) {
+  fa_status st = check_shape(B, H, N, d, scale, (int)FA_BF16);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (window < 0 || !std::isfinite(q_descale) || !std::isfinite(k_descale) ||
+      !std::isfinite(v_descale) || !(q_descale > 0.f) || !(k_descale > 0.f) ||
+      !(v_descale > 0.f))
+    return FA_ERR_INVALID_ARG;
+  const float qk = scale * q_descale * k_descale;
+  if (!std::isfinite(qk)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+      !aligned16(LSE))
+    return FA_ERR_INVALID_ARG;
+  int dev;
+  DeviceInfo info;
+  if ((st = current_device(&dev, &info)) != FA_OK) return st;
+  if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
+  if (window >= N) window = 0;
+  fa::AttnShape s{B, H, N, d, qk, (causal || window > 0) ? 1 : 0, window};
+  s.fp8 = 1;
+  s.v_descale = v_descale;
+  if ((st = get_encoder()) != FA_OK) return st;
+  fa::TileMaps maps;
+  const int BH = B * H;
+  if ((st = make_map_u8(&maps.q, Q, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map_u8(&maps.k, K, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map_u8(&maps.v, V, BH, N, d)) != FA_OK) return st;
+  return from_cuda(fa::launch_fwd_tc(s, maps, O, LSE, info.num_sms,
+                                     fa::kWaitLimitNs,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
 
 FA_API fa_status fa_fwd_dropout(const void* Q, const void* K, const void* V,
                                 void* O, float* LSE, int B, int H, int N, int d,

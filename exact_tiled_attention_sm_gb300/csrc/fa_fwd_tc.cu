@@ -33,7 +33,14 @@
 // own row's words, and P is written to TMEM with the dropped entries zeroed.
 // The row sum l stays that of the undropped row (so LSE is unchanged) and
 // the factor 256/(256 - t) of kept entries is folded into the final 1/l.
+//
+// The E8 variant takes Q, K, V as 8-bit E4M3 with per-tensor factors: the
+// same pipeline with 16 KiB tiles (d = 128 bytes per row), kind::f8f6f4 MMAs
+// (K = 32), and P written to TMEM as E4M3 (32 columns per S_t) scaled by
+// 2^8, so that the probabilities use the format's normal range; the 2^8 is
+// taken out again with 1/l (l sums the same scaled values) and the LSE.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "fa_internal.h"
 #include "fa_philox.cuh"
@@ -43,13 +50,14 @@
 namespace fa {
 namespace fwdtc {
 
-template <int D>
+template <int D, bool E8 = false>
 struct Cfg {
-  static constexpr int CH = D / 64;               // 128-byte column chunks
+  static constexpr int CH = E8 ? D / 128 : D / 64;  // 128-byte column chunks
+  static constexpr int CHUNK_ELEMS = E8 ? 128 : 64;
   static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = CH * CHUNK_BYTES;
-  static constexpr int KST = (D == 64) ? 4 : 2;   // K ring stages
-  static constexpr int VST = (D == 64) ? 4 : 2;   // V ring stages
+  static constexpr int KST = (CH == 1) ? 4 : 2;  // K ring stages
+  static constexpr int VST = (CH == 1) ? 4 : 2;  // V ring stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
@@ -69,8 +77,25 @@ struct Cfg {
   static constexpr uint32_t TM_S = 0;     // + 128 * t
   static constexpr uint32_t TM_O = 256;   // + D * t
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
-  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, 0, 1);
+  static constexpr uint32_t IDESC_S =
+      E8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
+  static constexpr uint32_t IDESC_PV =
+      E8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
+  // S = Q K^T for one query block and one key block
+  static __device__ __forceinline__ void mma_s(uint32_t d, uint32_t sq, uint32_t sk) {
+    if constexpr (E8)
+      mma_rows_x_rows_f8<D>(d, sq, sk, IDESC_S);
+    else
+      mma_rows_x_rows<D>(d, sq, sk, IDESC_S);
+  }
+  // O (+)= P V, P in TMEM
+  static __device__ __forceinline__ void mma_pv(uint32_t d, uint32_t p, uint32_t sv,
+                                                bool acc) {
+    if constexpr (E8)
+      mma_tmem_x_rows_f8(d, p, sv, IDESC_PV, acc);
+    else
+      mma_tmem_x_rows(d, p, sv, IDESC_PV, acc);
+  }
 };
 
 constexpr int kThreads = 320;
@@ -80,7 +105,8 @@ constexpr int kTmaWarp = 9;
 struct Params {
   __nv_bfloat16* O;
   float* LSE;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (times the Q and K factors for E8)
+  float v_descale;   // E8: the V factor
   uint64_t wait_limit_ns;
   DropSpec drop;     // used by the DR variant only
   FwdSched sched;
@@ -93,14 +119,15 @@ enum : uint32_t {
   SITE_ALIGN
 };
 
-// W: the causal sliding-window variant, DR: dropout (each compiled
-// separately, so that the plain kernels carry none of their bookkeeping).
-template <int D, bool W, bool DR>
+// W: the causal sliding-window variant, DR: dropout, E8: E4M3 inputs (each
+// compiled separately, so that the plain kernels carry none of their
+// bookkeeping).
+template <int D, bool W, bool DR, bool E8>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E8>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar0 = sb + C::OFF_BAR;
@@ -177,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < (valid1 ? 2 : 1); ++t)
           for (int c = 0; c < C::CH; ++c)
             tma_load_3d(sQ(t) + c * C::CHUNK_BYTES, &mq, bar(C::B_QFULL),
-                        c * 64, (q0 + t) * 128, bh);
+                        c * C::CHUNK_ELEMS, (q0 + t) * 128, bh);
         last_q = it & 1;
         bool ok = true;
         for (int j = jlo; j <= jhi && ok; ++j) {
@@ -193,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = sb + C::OFF_K + s * C::TILE_BYTES;
             for (int c = 0; c < C::CH; ++c)
               tma_load_3d(dst + c * C::CHUNK_BYTES, &mk, bar(C::B_KFULL + s),
-                          c * 64, j * 128, bh);
+                          c * C::CHUNK_ELEMS, j * 128, bh);
             k_used |= 1u << s;
             k_par = (k_par & ~(1u << s)) | (ph << s);
             ++kcnt;
@@ -210,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = sb + C::OFF_V + s * C::TILE_BYTES;
             for (int c = 0; c < C::CH; ++c)
               tma_load_3d(dst + c * C::CHUNK_BYTES, &mv, bar(C::B_VFULL + s),
-                          c * 64, j * 128, bh);
+                          c * C::CHUNK_ELEMS, j * 128, bh);
             v_used |= 1u << s;
             v_par = (v_par & ~(1u << s)) | (ph << s);
             ++vcnt;
@@ -269,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t)
             if (in_t(t, jlo)) {
-              mma_rows_x_rows<D>(tmem + C::TM_S + 128 * t, sQ(t), sk, C::IDESC_S);
+              C::mma_s(tmem + C::TM_S + 128 * t, sQ(t), sk);
               umma_commit(bar(C::B_SFULL + t));
             }
           umma_commit(bar(C::B_KEMPTY + s));
@@ -302,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               ++pc;
               tc_fence_after();
-              mma_tmem_x_rows(tmem + C::TM_O + D * t, tmem + C::TM_S + 128 * t,
-                              sv, C::IDESC_PV, j > (t ? lo1 : lo0));
+              C::mma_pv(tmem + C::TM_O + D * t, tmem + C::TM_S + 128 * t, sv,
+                        j > (t ? lo1 : lo0));
               if (j == (t ? hi1 : hi0)) umma_commit(bar(C::B_ODONE + t));
             }
             if (in_t(t, j + 1)) {
@@ -316,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 k_ready = true;
               }
-              mma_rows_x_rows<D>(tmem + C::TM_S + 128 * t, sQ(t), sk, C::IDESC_S);
+              C::mma_s(tmem + C::TM_S + 128 * t, sQ(t), sk);
               umma_commit(bar(C::B_SFULL + t));
             }
           }
@@ -425,7 +452,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = 2^(scale*log2(e)*s - mref): one packed fma per pair, row sum
         // in four packed accumulators
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t nm2 = f2_pack(-mref_new, -mref_new);
+        // (E8: 2^8 P, inside E4M3's normal range)
+        const float nref = E8 ? 8.f - mref_new : -mref_new;
+        const uint64_t nm2 = f2_pack(nref, nref);
         // O_t *= alpha is needed when a row of this warp moved its max (the
         // previous P V product into O_t completed before S_t of this block
         // did).  O's first 64 columns are requested (always, which keeps the
@@ -465,10 +494,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             a = ex2_approx(a);
             b = ex2_approx(b);
             acc[i & 3] = fadd2(acc[i & 3], f2_pack(a, b));
-            pk[i] = pack_bf16x2(a, b);
+            if constexpr (E8)
+              pk[i] = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                               __NV_E4M3);
+            else
+              pk[i] = pack_bf16x2(a, b);
             if constexpr (DR) pk[i] &= pair_mask(kw[i >> 1], i);
           }
-          tmem_st16(tS + 16 * h, pk);
+          if constexpr (E8) {  // four E4M3 values a column, key order
+            uint32_t p8[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) p8[w] = __byte_perm(pk[2 * w], pk[2 * w + 1], 0x5410);
+            tmem_st8(tS + 8 * h, p8);
+          } else {
+            tmem_st16(tS + 16 * h, pk);
+          }
         }
         float rs_lo, rs_hi;
         f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), rs_lo, rs_hi);
@@ -523,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ocnt;
       tc_fence_after();
       // kept entries carry the factor 256/(256 - t)
-      const float inv_l = (DR ? p.drop.keep_scale : 1.f) / l;
+      const float inv_l = (DR ? p.drop.keep_scale : E8 ? p.v_descale : 1.f) / l;
       const bool store = row < sc.N;
       __nv_bfloat16* orow = p.O + ((size_t)bh * sc.N + (size_t)(store ? row : 0)) * D;
 #pragma unroll
@@ -545,7 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (store)
-        p.LSE[(size_t)bh * sc.N + row] = (mref + log2f(l)) * 0.69314718055994531f;
+        p.LSE[(size_t)bh * sc.N + row] =
+            (mref - (E8 ? 8.f : 0.f) + log2f(l)) * 0.69314718055994531f;
       // all TMEM reads of O_t are done before the next item's first P V
       // product (ordered by this group's next p_ready arrival)
       tc_fence_before();
@@ -558,14 +599,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int D, bool W, bool DR>
+template <int D, bool W, bool DR, bool E8 = false>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
                    float* LSE, int num_sms, uint64_t lim, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E8>;
   static bool attr_done = false;  // per process; same value on every device
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(
-        fwd_kernel<D, W, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        fwd_kernel<D, W, DR, E8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done = true;
@@ -575,13 +616,14 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   p.LSE = LSE;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.wait_limit_ns = lim;
+  p.v_descale = s.v_descale;
   p.drop = s.drop;
   const int BH = s.B * s.H;
   FwdSched probe;
   probe.init(BH, s.N, s.causal, num_sms, s.window);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  fwd_kernel<D, W, DR><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
+  fwd_kernel<D, W, DR, E8><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
@@ -593,6 +635,9 @@ cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
                           cudaStream_t stream) {
   const int v = (s.window > 0 ? 1 : 0) + (s.drop.t4 != 0 ? 2 : 0);
   const uint64_t lim = wait_limit_ns;
+  if (s.fp8)  // d = 128, no dropout (checked by the caller)
+    return v & 1 ? fwdtc::launch<128, true, false, true>(s, maps, O, LSE, num_sms, lim, stream)
+                 : fwdtc::launch<128, false, false, true>(s, maps, O, LSE, num_sms, lim, stream);
 #define FA_FWD_CASE(DD)                                                        \
   switch (v) {                                                                 \
     case 0: return fwdtc::launch<DD, false, false>(s, maps, O, LSE, num_sms, lim, stream); \

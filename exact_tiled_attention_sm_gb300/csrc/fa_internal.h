@@ -25,6 +25,8 @@ struct AttnShape {
   int causal;
   int window = 0;  // > 0: causal sliding window of this many keys
   DropSpec drop{};
+  int fp8 = 0;           // Q, K, V are E4M3; `scale` includes their factors
+  float v_descale = 1.f; // fp8: the factor of V
 };
 
 // TMA descriptors (built by fa_api.cu): the bf16 [B*H, N, d] tensors with

@@ -86,6 +86,38 @@ __device__ __forceinline__ void mma_colsT_x_rows(uint32_t d_tmem, uint32_t sat,
     umma_ss(d_tmem, da + mstep(kk), db + mstep(kk), idesc, kk > 0 ? 1u : 0u);
 }
 
+// 8-bit (E4M3) tiles.  A [128][128] byte tile (d = 128) is one 16 KiB chunk
+// of the layout above, byte-for-byte like a 64-column bf16 chunk, and one MMA
+// consumes K = 32 elements = 32 bytes: the K-major steps are kstep's, four
+// per 128-byte row.
+// D(128 x 128) (+)= A B^T with A, B both [128][RowBytes] K-major byte tiles.
+template <int RowBytes>
+__device__ __forceinline__ void mma_rows_x_rows_f8(uint32_t d_tmem, uint32_t sa,
+                                                   uint32_t sb, uint32_t idesc) {
+  const uint64_t da = kdesc(sa), db = kdesc(sb);
+#pragma unroll
+  for (int kk = 0; kk < RowBytes / 32; ++kk)
+    umma_ss_f8(d_tmem, da + kstep(kk), db + kstep(kk), idesc, kk > 0 ? 1u : 0u);
+}
+
+// MN-major step kk of an 8-bit tile: 32 rows of 128 bytes.
+__host__ __device__ constexpr uint32_t mstep_f8(int kk) {
+  return (uint32_t)((kk * 32 * 128) >> 4);
+}
+
+// D(128 x 128) (+)= A B with A (128 x 128) in TMEM as E4M3 (four per 32-bit
+// column, lanes = rows; 8 columns per MMA) and B a [128][128] byte tile read
+// MN-major (4 MMAs of K = 32 rows).
+__device__ __forceinline__ void mma_tmem_x_rows_f8(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint32_t sb, uint32_t idesc,
+                                                   bool accumulate) {
+  const uint64_t db = mdesc(sb);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    umma_ts_f8(d_tmem, a_tmem + kk * 8, db + mstep_f8(kk), idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // Byte offset of the 16-byte piece `p` (0..15 across a 128-element row) of
 // row r in the layout above.
 __device__ __forceinline__ uint32_t swz_offset(int r, int p) {

@@ -209,6 +209,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn,
          ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f8f6f4 with both operands E4M3 (format
+// code 0 in the A and B fields) and an fp32 accumulator; the other fields as
+// in idesc_bf16_f32.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn,
+                                                      int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100-family version.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 version (1), 49-51 base offset (0:
@@ -249,6 +258,31 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem,
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same two forms for 8-bit operands (kind::f8f6f4, K = 32 per MMA).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t adesc,
+                                           uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem,
+                                           uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
           d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
@@ -301,6 +335,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr,
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
       "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]),
       "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// 32 lanes x 8 columns of 32 bits.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7])
       : "memory");
 }
 

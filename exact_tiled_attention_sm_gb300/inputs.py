@@ -75,6 +75,33 @@ def workload_inputs(w: Workload, with_dO=None):
     return seeded_inputs(w.B, w.H, w.N, w.d, w.seed, w.dtype, with_dO)
 
 
+E4M3_MAX = 448.0  # largest finite OCP FP8 E4M3 value
+
+
+def e4m3_inputs(B, H, N, d, seed):
+    """Q, K, V as E4M3 with per-tensor factors, for the 8-bit forward: the
+    fp32 draws of ``seeded_inputs`` (same seed, same order), each divided by
+    its factor amax/448 (rounded to an fp32 value, which both sides then use
+    exactly) and rounded to E4M3 by torch (round to nearest even).
+    Returns ({"Q": q8, "K": k8, "V": v8} as torch.float8_e4m3fn CPU tensors,
+    {"Q": qd, "K": kd, "V": vd} the factors)."""
+    x = seeded_inputs(B, H, N, d, seed, dtype="f32")
+    out, fac = {}, {}
+    for n in ("Q", "K", "V"):
+        amax = float(x[n].abs().max())
+        f = float(torch.tensor(amax / E4M3_MAX if amax > 0 else 1.0,
+                               dtype=torch.float32))
+        out[n] = (x[n] / f).to(torch.float8_e4m3fn)
+        fac[n] = f
+    return out, fac
+
+
+def e4m3_to_f64(t, factor):
+    """The values an E4M3 tensor stands for: exact widening times its factor
+    (one rounding of the product in float64)."""
+    return t.detach().to("cpu").to(torch.float32).to(torch.float64).numpy() * factor
+
+
 def to_f64(t):
     """Exact widening of a bf16/fp32 tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()

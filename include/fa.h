@@ -149,6 +149,26 @@ fa_status fa_dropout_mask(unsigned char* keep, int B, int H, int N,
                           float dropout_p, unsigned long long seed,
                           void* stream);
 
+/* Forward pass with 8-bit inputs (the low-precision arithmetic the pages
+ * credit to FlashAttention-3: "LLM Architecture Refresh [3]", section 8;
+ * "FlashAttention from scratch", "Trade-offs and edge cases").
+ * Q, K, V are OCP FP8 E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities), [B][H][N][d], standing for q_descale * Q,
+ * k_descale * K and v_descale * V.  Computes the attention of those values:
+ * S = scale * q_descale * k_descale * (Q K^T) with exact 8-bit products and
+ * fp32 accumulation, P = exp(S - rowmax) rounded to E4M3 (times 2^8) for the
+ * P V product, O = v_descale * (P V) / rowsum(P) written as bf16, and LSE
+ * (fp32, natural log) as in fa_fwd.  causal and window as in
+ * fa_fwd_dropout.  The rounding of P to E4M3 (3 mantissa bits) bounds the
+ * error of O by about 2^-4 * sum_k p_k |v_k| per element.
+ * Errors: FA_ERR_UNSUPPORTED for d != 128 or a device other than sm_103;
+ * FA_ERR_INVALID_ARG for non-positive or non-finite factors, window < 0, and
+ * the shape and alignment errors of fa_fwd. */
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O,
+                     float* LSE, int B, int H, int N, int d, float scale,
+                     int causal, int window, float q_descale, float k_descale,
+                     float v_descale, void* stream);
+
 /* Size of the device scratch array that fa_bwd_noalloc uses in place of a
  * caller workspace: 64 MiB, statically reserved on every GPU that loads the
  * library (the reservation lasts until the process exits). */

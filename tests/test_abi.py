@@ -167,6 +167,17 @@ def test_dropout_entry_points_reject_bad_arguments(L):
         assert fa.fa_dropout_mask(*args, None) == fa.FA_ERR_INVALID_ARG
 
 
+def test_fp8_entry_point_rejects_bad_arguments(L):
+    a = [16, 16, 16, 16, 16, 1, 1, 16]
+    for d, f, w, expect in ((64, (1.0, 1.0, 1.0), 0, fa.FA_ERR_UNSUPPORTED),
+                            (128, (0.0, 1.0, 1.0), 0, fa.FA_ERR_INVALID_ARG),
+                            (128, (1.0, float("inf"), 1.0), 0, fa.FA_ERR_INVALID_ARG),
+                            (128, (1.0, 1.0, -2.0), 0, fa.FA_ERR_INVALID_ARG),
+                            (128, (1.0, 1.0, 1.0), -1, fa.FA_ERR_INVALID_ARG),
+                            (128, (1e30, 1e30, 1.0), 0, fa.FA_ERR_INVALID_ARG)):
+        assert fa.fa_fwd_fp8(*a, d, 0.1, 0, w, *f, None) == expect
+
+
 def test_library_has_no_oracle_symbols(L):
     """The product library and the oracle share nothing."""
     assert not hasattr(L, "oracle_fwd")

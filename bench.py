@@ -184,7 +184,8 @@ def run_profile(args):
     """Only the launches of one workload (for ncu): W warm-up steps then K
     steps, nothing else on the GPU.  `train_fwd_bwd` runs fa_fwd + fa_bwd
     (4 launches a step); a forward workload runs fa_fwd (1 launch a step).
-    --window and --dropout select those variants."""
+    --window and --dropout select those variants, --fp8 the 8-bit forward
+    (forward workloads only)."""
     import torch
     import exact_tiled_attention_sm_gb300 as fa
     from exact_tiled_attention_sm_gb300 import inputs
@@ -200,7 +201,14 @@ def run_profile(args):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = fa.workspace(w.B, w.H, w.N, w.d)
     opt = {"window": args.window, "dropout_p": args.dropout, "seed": 1234}
-    for _ in range(args.warmup + args.steps):
+    if args.fp8:
+        x8, fac = inputs.e4m3_inputs(w.B, w.H, w.N, w.d, w.seed)
+        q8, k8, v8 = (x8[n].cuda() for n in ("Q", "K", "V"))
+        dsc = (fac["Q"], fac["K"], fac["V"])
+        for _ in range(args.warmup + args.steps):
+            fa.fwd_fp8(q8, k8, v8, w.scale, dsc, causal, out=o, lse=lse,
+                       window=args.window)
+    for _ in range(0 if args.fp8 else args.warmup + args.steps):
         fa.fwd(q, k, v, w.scale, causal, out=o, lse=lse, **opt)
         if w.passes == "fwd+bwd":
             fa.bwd(q, k, v, o, do, lse, w.scale, causal, dq=dq, dk=dk, dv=dv, ws=ws,
@@ -210,7 +218,8 @@ def run_profile(args):
     if st != fa.FA_OK:
         raise SystemExit(f"device status: {fa.status_string(st)}")
     return {"profile": args.workload, "causal": causal, "steps": args.steps,
-            "warmup": args.warmup, "window": args.window, "dropout": args.dropout}
+            "warmup": args.warmup, "window": args.window, "dropout": args.dropout,
+            "fp8": bool(args.fp8)}
 
 
 # --------------------------------------------------------------------- ours
@@ -600,6 +609,7 @@ def main():
     ap.add_argument("--causal", type=int, default=1)
     ap.add_argument("--window", type=int, default=0, help="profile: sliding window")
     ap.add_argument("--dropout", type=float, default=0.0, help="profile: dropout p")
+    ap.add_argument("--fp8", action="store_true", help="profile: the 8-bit forward")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.profile:

@@ -453,6 +453,19 @@ def run_ours(args):
                 "launches": reps}
             launches += reps
         del q8, k8, v8, of, lf
+    # --- head dimension 256: the tensor-core forward (one query block per
+    # item) both ways, and the training step at d = 256, whose backward runs
+    # on the CUDA cores
+    d256_results = {}
+    for name, causal_v, passes in (("d256_fwd", False, "fwd"), ("d256_fwd", True, "fwd"),
+                                   ("d256_train", True, "fwd+bwd")):
+        wf = inputs.WORKLOADS[name]
+        ms, nl = time_variant(name, passes, causal_v)
+        fl = attn_flops(wf.B, wf.H, wf.N, wf.d, causal_v, passes)
+        d256_results[f"{name}{'_causal' if causal_v else ''}_{passes.replace('+', '_')}"] = {
+            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "launches": nl}
+        launches += nl
     clocks = sampler.stop()
     st = fa.last_device_status()
     if st != fa.FA_OK:
@@ -468,7 +481,7 @@ def run_ours(args):
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = attn_flops(B, H, N, d, causal, "fwd") / (fwd_ms * 1e-3) / 1e12
     for r in (list(fwd_results.values()) + list(window_results.values())
-              + list(dropout_results.values())):
+              + list(dropout_results.values()) + list(d256_results.values())):
         r["frac_of_peak"] = round(r["tflops"] / world / peak, 4)
     for r in fp8_results.values():  # against the 8-bit peak: 2x the bf16 one
         r["frac_of_fp8_peak"] = round(r["tflops"] / world / (2 * peak), 4)
@@ -515,6 +528,7 @@ def run_ours(args):
         "window": window_results,
         "dropout": dropout_results,
         "fp8": fp8_results,
+        "d256": d256_results,
         "fp8_peak_note": "8-bit dense peak taken as 2 x the measured bf16 burst peak (the nominal 4.5 / 2.25 PFLOP/s ratio)",
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),

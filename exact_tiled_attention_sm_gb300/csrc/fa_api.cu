@@ -124,7 +124,7 @@ fa_status check_shape(int B, int H, int N, int d, float scale, int dt) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (dt != FA_BF16 && dt != FA_F32) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   const long long elems = (long long)B * H * N * d;
   if (elems >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   if ((long long)B * H >= (1ll << 31) / 128) return FA_ERR_INVALID_ARG;
@@ -182,12 +182,16 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
         s, static_cast<const float*>(Q), static_cast<const float*>(K),
         static_cast<const float*>(V), static_cast<float*>(O), LSE, cs));
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
+  if (d == 256 && drop.t4 != 0) return FA_ERR_UNSUPPORTED;  // no bf16 d = 256 dropout
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TileMaps maps;
   const int BH = B * H;
   if ((st = make_map(&maps.q, Q, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
+  if (d == 256)
+    return from_cuda(fa::launch_fwd256_tc(s, maps, O, LSE, info.num_sms,
+                                          fa::kWaitLimitNs, cs));
   return from_cuda(fa::launch_fwd_tc(s, maps, O, LSE, info.num_sms,
                                      fa::kWaitLimitNs, cs));
 }
@@ -320,6 +324,13 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
         static_cast<float*>(dV), cs));
   }
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
+  if (d == 256) {  // CUDA cores: the tensor-core backward's TMEM does not fit
+    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
+    if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, nullptr, cs))) != FA_OK)
+      return st;
+    return from_cuda(fa::launch_bwd_simt_bf16(s, Q, K, V, dO, LSE, Dvec, dQ, dK,
+                                              dV, cs));
+  }
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TileMaps maps;
   const int BH = B * H;
@@ -377,7 +388,8 @@ FA_API fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V,
 
 FA_API fa_status fa_last_device_status(void* stream) {
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const unsigned int words[3] = {fa::read_status_fwd_tc(cs),
+  const unsigned int words[4] = {fa::read_status_fwd_tc(cs),
+                                 fa::read_status_fwd256_tc(cs),
                                  fa::read_status_bwd_tc(cs),
                                  fa::read_status_simt(cs)};
   fa_status out = FA_OK;

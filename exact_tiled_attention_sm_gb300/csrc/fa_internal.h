@@ -43,6 +43,12 @@ cudaError_t launch_fwd_tc(const AttnShape& s, const TileMaps& maps, void* O,
                           cudaStream_t stream);
 unsigned int read_status_fwd_tc(cudaStream_t stream);
 
+// fa_fwd256_tc.cu -- bf16 forward for d = 256 (one query block per item).
+cudaError_t launch_fwd256_tc(const AttnShape& s, const TileMaps& maps, void* O,
+                             float* LSE, int num_sms, uint64_t wait_limit_ns,
+                             cudaStream_t stream);
+unsigned int read_status_fwd256_tc(cudaStream_t stream);
+
 // fa_bwd_tc.cu -- bf16 backward on tcgen05/TMEM.
 cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
                           const float* LSE, const float* Dvec, float* dQacc,
@@ -59,6 +65,12 @@ cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
                            const float* V, const float* dO, const float* LSE,
                            const float* Dvec, float* dQ, float* dK, float* dV,
                            cudaStream_t stream);
+// bf16 backward on the CUDA cores for d = 256 (fp32 arithmetic), where the
+// tensor-core backward's TMEM layout does not fit.
+cudaError_t launch_bwd_simt_bf16(const AttnShape& s, const void* Q, const void* K,
+                                 const void* V, const void* dO, const float* LSE,
+                                 const float* Dvec, void* dQ, void* dK, void* dV,
+                                 cudaStream_t stream);
 // D = rowsum(dO * O) (fp32), and dQacc zeroed when non-null.
 cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
                            int is_bf16, float* Dvec, float* dQacc,

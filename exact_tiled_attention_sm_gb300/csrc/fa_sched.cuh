@@ -1,7 +1,8 @@
 // fa_sched.cuh -- the forward kernel's causal tile scheduler (host + device).
 //
 // A work item is one head (b, h) and one pair of consecutive 128-row query
-// blocks (rows [256*pair, 256*pair + 256)).  For query block q, the key
+// blocks (rows [256*pair, 256*pair + 256)), or one query block for kernels
+// that hold a single block (blocks_per_item = 1; "pair" is then the block).  For query block q, the key
 // blocks visited are j = kv_lo(q) .. kv_hi(q): all of them without a mask;
 // up to the diagonal (kv_hi = q) under the causal mask, where a key block
 // whose first key lies after the query block's last row is never loaded or
@@ -42,8 +43,10 @@ struct FwdSched {
   int n_q_tiles, n_pairs, n_kv_total, group, total_items;
 
   // window > 0: causal sliding window of `window` keys (implies causal).
+  // n_pairs counts the items of one head (pairs, or blocks when
+  // blocks_per_item = 1).
   __host__ __device__ void init(int bh, int n, int is_causal, int grid_size,
-                                int win = 0) {
+                                int win = 0, int blocks_per_item = 2) {
     BH = bh;
     N = n;
     window = win > 0 ? win : 0;
@@ -51,7 +54,7 @@ struct FwdSched {
     grid = grid_size;
     n_q_tiles = (N + 127) / 128;
     n_kv_total = n_q_tiles;
-    n_pairs = (n_q_tiles + 1) / 2;
+    n_pairs = (n_q_tiles + blocks_per_item - 1) / blocks_per_item;
     int g = (causal ? kGroupWaves : 1) * grid / n_pairs;
     if (g < 1) g = 1;
     if (g > BH) g = BH;

@@ -35,14 +35,22 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Loads rows [r0, r0+32) of one head into shared memory with row stride
-// `ld`, zero-filling rows >= N.
-template <int D>
-__device__ __forceinline__ void load_rows(float* dst, int ld, const float* src,
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Loads rows [r0, r0+32) of one head into shared memory (as fp32) with row
+// stride `ld`, zero-filling rows >= N.
+template <int D, typename T>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const T* src,
                                           int r0, int N) {
   for (int i = threadIdx.x; i < kRows * D; i += blockDim.x) {
     const int r = i / D, c = i % D;
-    dst[r * ld + c] = (r0 + r < N) ? src[(size_t)(r0 + r) * D + c] : 0.f;
+    dst[r * ld + c] = (r0 + r < N) ? to_f(src[(size_t)(r0 + r) * D + c]) : 0.f;
   }
 }
 
@@ -119,13 +127,15 @@ __global__ void __launch_bounds__(128)
 
 // dK, dV for 32 keys per CTA (8 per warp); lane = query within a 32-query
 // block.  P is recomputed from LSE: p = exp(scale*<q,k> - LSE)
-// ("FlashAttention from scratch", follow-up on the backward pass).
-template <int D>
+// ("FlashAttention from scratch", follow-up on the backward pass).  T: the
+// tensors' type (fp32, or bf16 where no tensor-core backward exists);
+// arithmetic in fp32 either way.
+template <int D, typename T>
 __global__ void __launch_bounds__(128)
-    bwd_f32_dkdv_kernel(const float* __restrict__ Q, const float* __restrict__ K,
-                        const float* __restrict__ V, const float* __restrict__ dO,
+    bwd_f32_dkdv_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                        const T* __restrict__ V, const T* __restrict__ dO,
                         const float* __restrict__ LSE, const float* __restrict__ Dv,
-                        float* __restrict__ dK, float* __restrict__ dV, int N,
+                        T* __restrict__ dK, T* __restrict__ dV, int N,
                         float scale, int causal, int window, const DropSpec drop) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
@@ -191,19 +201,19 @@ __global__ void __launch_bounds__(128)
     if (key >= N) continue;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      dV[head + (size_t)key * D + c * 32 + lane] = av[i][c] * drop.keep_scale;
-      dK[head + (size_t)key * D + c * 32 + lane] = ak[i][c] * scale;
+      dV[head + (size_t)key * D + c * 32 + lane] = from_f<T>(av[i][c] * drop.keep_scale);
+      dK[head + (size_t)key * D + c * 32 + lane] = from_f<T>(ak[i][c] * scale);
     }
   }
 }
 
 // dQ for 32 query rows per CTA: dQ_r = scale * sum_k dS_rk k_k.
-template <int D>
+template <int D, typename T>
 __global__ void __launch_bounds__(128)
-    bwd_f32_dq_kernel(const float* __restrict__ Q, const float* __restrict__ K,
-                      const float* __restrict__ V, const float* __restrict__ dO,
+    bwd_f32_dq_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                      const T* __restrict__ V, const T* __restrict__ dO,
                       const float* __restrict__ LSE, const float* __restrict__ Dv,
-                      float* __restrict__ dQ, int N, float scale, int causal,
+                      T* __restrict__ dQ, int N, float scale, int causal,
                       int window, const DropSpec drop) {
   constexpr int LD = D + 1;
   extern __shared__ float sm[];
@@ -264,7 +274,7 @@ __global__ void __launch_bounds__(128)
     if (row >= N) continue;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c)
-      dQ[head + (size_t)row * D + c * 32 + lane] = acc[rr][c] * scale;
+      dQ[head + (size_t)row * D + c * 32 + lane] = from_f<T>(acc[rr][c] * scale);
   }
 }
 
@@ -366,23 +376,22 @@ static cudaError_t fwd_f32_launch(const AttnShape& s, const float* Q,
   return cudaGetLastError();
 }
 
-template <int D>
-static cudaError_t bwd_f32_launch(const AttnShape& s, const float* Q,
-                                  const float* K, const float* V,
-                                  const float* dO, const float* LSE,
-                                  const float* Dvec, float* dQ, float* dK,
-                                  float* dV, cudaStream_t stream) {
+template <int D, typename T>
+static cudaError_t bwd_f32_launch(const AttnShape& s, const T* Q, const T* K,
+                                  const T* V, const T* dO, const float* LSE,
+                                  const float* Dvec, T* dQ, T* dK, T* dV,
+                                  cudaStream_t stream) {
   constexpr int bytes = (2 * simt::kRows * (D + 1) + 2 * simt::kKeys * D) * 4;
-  static cudaError_t a1 = smem_attr(simt::bwd_f32_dkdv_kernel<D>, bytes);
-  static cudaError_t a2 = smem_attr(simt::bwd_f32_dq_kernel<D>, bytes);
+  static cudaError_t a1 = smem_attr(simt::bwd_f32_dkdv_kernel<D, T>, bytes);
+  static cudaError_t a2 = smem_attr(simt::bwd_f32_dq_kernel<D, T>, bytes);
   if (a1 != cudaSuccess) return a1;
   if (a2 != cudaSuccess) return a2;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
-  simt::bwd_f32_dkdv_kernel<D><<<grid, 128, bytes, stream>>>(
+  simt::bwd_f32_dkdv_kernel<D, T><<<grid, 128, bytes, stream>>>(
       Q, K, V, dO, LSE, Dvec, dK, dV, s.N, s.scale, s.causal, s.window, s.drop);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  simt::bwd_f32_dq_kernel<D><<<grid, 128, bytes, stream>>>(
+  simt::bwd_f32_dq_kernel<D, T><<<grid, 128, bytes, stream>>>(
       Q, K, V, dO, LSE, Dvec, dQ, s.N, s.scale, s.causal, s.window, s.drop);
   return cudaGetLastError();
 }
@@ -391,6 +400,7 @@ cudaError_t launch_fwd_f32(const AttnShape& s, const float* Q, const float* K,
                            const float* V, float* O, float* LSE,
                            cudaStream_t stream) {
   if (s.d == 64) return fwd_f32_launch<64>(s, Q, K, V, O, LSE, stream);
+  if (s.d == 256) return fwd_f32_launch<256>(s, Q, K, V, O, LSE, stream);
   return fwd_f32_launch<128>(s, Q, K, V, O, LSE, stream);
 }
 
@@ -400,7 +410,20 @@ cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
                            cudaStream_t stream) {
   if (s.d == 64)
     return bwd_f32_launch<64>(s, Q, K, V, dO, LSE, Dvec, dQ, dK, dV, stream);
+  if (s.d == 256)
+    return bwd_f32_launch<256>(s, Q, K, V, dO, LSE, Dvec, dQ, dK, dV, stream);
   return bwd_f32_launch<128>(s, Q, K, V, dO, LSE, Dvec, dQ, dK, dV, stream);
+}
+
+cudaError_t launch_bwd_simt_bf16(const AttnShape& s, const void* Q, const void* K,
+                                 const void* V, const void* dO, const float* LSE,
+                                 const float* Dvec, void* dQ, void* dK, void* dV,
+                                 cudaStream_t stream) {
+  using B = __nv_bfloat16;
+  return bwd_f32_launch<256>(s, static_cast<const B*>(Q), static_cast<const B*>(K),
+                             static_cast<const B*>(V), static_cast<const B*>(dO),
+                             LSE, Dvec, static_cast<B*>(dQ), static_cast<B*>(dK),
+                             static_cast<B*>(dV), stream);
 }
 
 cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
@@ -413,6 +436,8 @@ cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
     auto g = reinterpret_cast<const __nv_bfloat16*>(dO);
     if (s.d == 64)
       simt::bwd_pre_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
+    else if (s.d == 256)
+      simt::bwd_pre_kernel<256, __nv_bfloat16><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
     else
       simt::bwd_pre_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
   } else {
@@ -420,6 +445,8 @@ cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
     auto g = reinterpret_cast<const float*>(dO);
     if (s.d == 64)
       simt::bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
+    else if (s.d == 256)
+      simt::bwd_pre_kernel<256, float><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
     else
       simt::bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(o, g, Dvec, dQacc, rows);
   }

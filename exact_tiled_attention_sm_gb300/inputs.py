@@ -53,6 +53,12 @@ WORKLOADS = {
                        "fwd", 1003 + 32768),
     "train_fwd_bwd": _w("train_fwd_bwd", 8, 16, 2048, 128, "bf16", (True,),
                         "fwd+bwd", 1004),
+    # head dimension 256 (the d^2/M wall): a 4096-token forward, and the
+    # training step's shape at d = 256
+    "d256_fwd": _w("d256_fwd", 2, 16, 4096, 256, "bf16", (False, True), "fwd",
+                   1005),
+    "d256_train": _w("d256_train", 4, 16, 2048, 256, "bf16", (True,),
+                     "fwd+bwd", 1006),
 }
 
 

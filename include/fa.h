@@ -29,8 +29,15 @@
  *     natural log.
  *   - dt = FA_BF16: bf16 inputs, fp32 accumulation on the tensor cores.
  *     dt = FA_F32: fp32 inputs and arithmetic throughout (CUDA cores).
- *   - d must be 64 or 128; N >= 1; B, H >= 1; B*H*N*d must fit in 2^31
- *     elements per tensor; scale must be finite.
+ *   - d must be 64, 128 or 256; N >= 1; B, H >= 1; B*H*N*d must fit in
+ *     2^31 elements per tensor; scale must be finite.
+ *   - d = 256 (the d^2/M wall of "Flash Attention, From First Principles",
+ *     "The rent arithmetic": one query block's S and O fill the tensor
+ *     memory): the bf16 forward runs on the tensor cores with one 128-row
+ *     query block per work item; the bf16 backward runs on the CUDA cores in
+ *     fp32 arithmetic (its tensor-core layout would need 768 TMEM columns);
+ *     fp32 inputs run on the CUDA cores as for every d; bf16 dropout at
+ *     d = 256 is FA_ERR_UNSUPPORTED.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  The returned status covers argument checks and the
  *     launch only; device-side failures (a bounded wait that ran out) are
@@ -50,7 +57,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned, bad scale  */
-  FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, unknown dtype, no sm_103a  */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64,128,256}, unknown dtype, no sm_103a */
   FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed              */
   FA_ERR_TIMEOUT = 4      /* a device-side bounded wait ran out             */
 } fa_status;

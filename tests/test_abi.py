@@ -55,7 +55,8 @@ def _fwd(**kw):
     (dict(B=0), fa.FA_ERR_INVALID_ARG),
     (dict(H=-1), fa.FA_ERR_INVALID_ARG),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
     (dict(dt=7), fa.FA_ERR_UNSUPPORTED),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),

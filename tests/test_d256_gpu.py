@@ -1,0 +1,175 @@
+"""Head dimension 256 against the fp64 oracle: the tensor-core bf16 forward
+(one query block per work item, S double-buffered in TMEM), the CUDA-core
+bf16 backward, and the fp32 path, with the library's tolerances (bf16 O
+<= 1e-2, LSE <= 1e-3, gradients relative L2 <= 1e-2, fp32 <= 1e-5)."""
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_sm_gb300 as fa
+import oracle
+from exact_tiled_attention_sm_gb300 import inputs
+from tests import helpers as h
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd(x, scale, causal, window=0):
+    q, k, v = (x[n].to("cuda") for n in ("Q", "K", "V"))
+    B, H, N, d = q.shape
+    o, ob = h.guarded((B, H, N, d), q.dtype)
+    lse, lb = h.guarded((B, H, N), torch.float32)
+    fa.fwd(q, k, v, scale, causal, out=o, lse=lse, window=window)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    assert h.guards_intact(ob) and h.guards_intact(lb), "write outside O/LSE"
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    return h.np64(o), h.np64(lse)
+
+
+def run_fwd_bwd(x, scale, causal, window=0):
+    q, k, v, do = (x[n].to("cuda") for n in ("Q", "K", "V", "dO"))
+    B, H, N, d = q.shape
+    o, lse = fa.fwd(q, k, v, scale, causal, window=window)
+    outs = [h.guarded((B, H, N, d), q.dtype) for _ in range(3)]
+    ws = fa.workspace(B, H, N, d)
+    ws.fill_(0xFF)
+    fa.bwd(q, k, v, o, do, lse, scale, causal, dq=outs[0][0], dk=outs[1][0],
+           dv=outs[2][0], ws=ws, window=window)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    for t, b in outs:
+        assert h.guards_intact(b), "write outside a gradient tensor"
+        assert torch.isfinite(t.float()).all()
+    return tuple(h.np64(t) for t, _ in outs)
+
+
+def f64(x, names):
+    return [inputs.to_f64(x[n]) for n in names]
+
+
+def check_grads(got, ref, tol=h.TOL_GRAD_REL):
+    errs = [h.rel_l2(g, r) for g, r in zip(got, ref)]
+    assert max(errs) <= tol, dict(zip(("dQ", "dK", "dV"), errs))
+    return errs
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 7, 127, 128, 129, 255, 300, 513])
+def test_bf16_forward_small_ragged(N, causal):
+    x = h.seeded(2, 2, N, 256, seed=3000 + N)
+    sc = 256 ** -0.5
+    o, lse = run_fwd(x, sc, causal)
+    O, L = oracle.fwd(*f64(x, ("Q", "K", "V")), sc, causal)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("N,w", [(300, 16), (513, 200), (700, 129), (1000, 1)])
+def test_bf16_forward_window(N, w):
+    x = h.seeded(1, 2, N, 256, seed=3100 + N + w)
+    if w < 16:  # a window of a few keys copies rows of V (see the window tests)
+        x["V"] = (x["V"].float() * 0.25).to(torch.bfloat16)
+    sc = 256 ** -0.5
+    o, lse = run_fwd(x, sc, True, window=w)
+    O, L = oracle.fwd(*f64(x, ("Q", "K", "V")), sc, True, window=w)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+def test_later_block_holds_the_max():
+    """Rows whose maximum arrives in a later key block rescale O (both column
+    halves of the row must agree on the maximum)."""
+    x = h.seeded(1, 2, 640, 256, seed=3200)
+    k = x["K"].float()
+    k[:, :, 500:520] *= 3.0
+    x["K"] = k.to(torch.bfloat16)
+    sc = 256 ** -0.5
+    o, lse = run_fwd(x, sc, False)
+    O, L = oracle.fwd(*f64(x, ("Q", "K", "V")), sc, False)
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_forward_full_size_sampled(causal):
+    w = inputs.WORKLOADS["d256_fwd"]
+    x = inputs.workload_inputs(w, with_dO=False)
+    o, lse = run_fwd(x, w.scale, causal)
+    rows = inputs.sample_rows(w.B, w.H, w.N, per_head=24, seed=w.seed).numpy()
+    O, L = oracle.fwd_rows(*f64(x, ("Q", "K", "V")), w.scale, causal, rows)
+    assert h.max_abs(o.reshape(-1, w.d)[rows], O) <= h.TOL_O_BF16
+    assert h.max_abs(lse.reshape(-1)[rows], L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [7, 129, 300])
+def test_bf16_backward_small(N, causal):
+    x = h.seeded(1, 2, N, 256, seed=3300 + N, with_dO=True)
+    sc = 256 ** -0.5
+    got = run_fwd_bwd(x, sc, causal)
+    dQ, dK, dV, _ = oracle.bwd(*f64(x, ("Q", "K", "V", "dO")), sc, causal)
+    check_grads(got, (dQ, dK, dV))
+
+
+def test_bf16_backward_window():
+    x = h.seeded(1, 2, 500, 256, seed=3400, with_dO=True)
+    sc = 256 ** -0.5
+    got = run_fwd_bwd(x, sc, True, window=150)
+    dQ, dK, dV, _ = oracle.bwd(*f64(x, ("Q", "K", "V", "dO")), sc, True, window=150)
+    check_grads(got, (dQ, dK, dV))
+
+
+def test_training_shape_sampled_heads():
+    """4 x 16 heads, N = 2048, d = 256, causal: two heads in full."""
+    w = inputs.WORKLOADS["d256_train"]
+    x = inputs.workload_inputs(w)
+    dq, dk, dv = run_fwd_bwd(x, w.scale, True)
+    g = np.random.default_rng(w.seed)
+    for bh in sorted(g.choice(w.B * w.H, size=2, replace=False).tolist()):
+        b, hh = divmod(bh, w.H)
+        sub = {n: x[n][b:b + 1, hh:hh + 1] for n in ("Q", "K", "V", "dO")}
+        dQ, dK, dV, _ = oracle.bwd(*f64(sub, ("Q", "K", "V", "dO")), w.scale, True)
+        check_grads((dq[b:b + 1, hh:hh + 1], dk[b:b + 1, hh:hh + 1],
+                     dv[b:b + 1, hh:hh + 1]), (dQ, dK, dV))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32(causal):
+    x = h.seeded(1, 2, 200, 256, seed=3500, dtype="f32", with_dO=True)
+    sc = 256 ** -0.5
+    o, lse = run_fwd(x, sc, causal)
+    Q, K, V, dO = f64(x, ("Q", "K", "V", "dO"))
+    O, L = oracle.fwd(Q, K, V, sc, causal)
+    assert h.max_abs(o, O) <= h.TOL_F32 and h.max_abs(lse, L) <= h.TOL_F32
+    got = run_fwd_bwd(x, sc, causal)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, causal)
+    errs = check_grads(got, (dQ, dK, dV))
+    assert max(errs) < 1e-5
+
+
+def test_dropout_is_unsupported_at_d256():
+    q = torch.zeros((1, 1, 16, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FAError):
+        fa.fwd(q, q, q, 1.0, dropout_p=0.1, seed=1)
+
+
+def test_repeated_runs_are_bit_identical():
+    """The forward has no atomics: any difference between runs is a race (a
+    wait that let a read overtake the tensor core).  Many items per CTA, many
+    key blocks per row."""
+    x = h.seeded(2, 16, 1024, 256, seed=3600)
+    q, k, v = (x[n].to("cuda") for n in ("Q", "K", "V"))
+    ref = None
+    for _ in range(4):
+        o, lse = fa.fwd(q, k, v, 0.0625, False)
+        torch.cuda.synchronize()
+        cur = (o.clone(), lse.clone())
+        if ref is None:
+            ref = cur
+        else:
+            assert torch.equal(ref[0], cur[0]) and torch.equal(ref[1], cur[1])
+    O, L = oracle.fwd_rows(*f64(x, ("Q", "K", "V")), 0.0625, False,
+                           inputs.sample_rows(2, 16, 1024, per_head=32, seed=1).numpy())
+    rows = inputs.sample_rows(2, 16, 1024, per_head=32, seed=1).numpy()
+    assert h.max_abs(h.np64(ref[0]).reshape(-1, 256)[rows], O) <= h.TOL_O_BF16

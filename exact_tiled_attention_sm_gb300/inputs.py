@@ -75,6 +75,18 @@ def seeded_inputs(B, H, N, d, seed, dtype="bf16", with_dO=False):
     return out
 
 
+def seeded_inputs_cuda(B, H, N, d, seed, with_dO=False):
+    """For tensors too large to draw on the host in reasonable time: Q, K, V
+    (and dO) as bf16 CUDA tensors drawn by torch's seeded CUDA generator
+    (``torch.randn`` in bf16, same order).  The oracle is given exact copies
+    of the heads it checks."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(int(seed))
+    names = ["Q", "K", "V"] + (["dO"] if with_dO else [])
+    return {n: torch.randn((B, H, N, d), generator=g, device="cuda",
+                           dtype=torch.bfloat16) for n in names}
+
+
 def workload_inputs(w: Workload, with_dO=None):
     if with_dO is None:
         with_dO = w.passes == "fwd+bwd"

@@ -313,9 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         const float mo = xch[(buf * 2 + (g ^ 1)) * 128 + rb];
+        // the exponent reference moves only when the maximum has risen by
+        // more than 8 (log2 units) or the row had nothing visible before, so
+        // that P < 2^8 and O is rarely rescaled; O / l and the LSE do not
+        // depend on the reference
+        const float m_prev = m;
         m = fmax3(m, mp, mo);
-        const float mref_new = (m == -INFINITY) ? 0.f : m * sl2;
-        const float alpha = ex2_approx(mref - mref_new);
+        const float cand = (m == -INFINITY) ? 0.f : m * sl2;
+        const bool move = (m_prev == -INFINITY) || (cand > mref + 8.f);
+        const float mref_new = move ? cand : mref;
+        const float alpha = move ? ex2_approx(mref - mref_new) : 1.f;
         mref = mref_new;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t nm2 = f2_pack(-mref_new, -mref_new);

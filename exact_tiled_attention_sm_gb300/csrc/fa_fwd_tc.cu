@@ -442,12 +442,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[i + k], x[i + 8 + k]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], x[120 + k]);
+        const float m_prev = m;
         m = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]),
                   fmax3(mk[6], mk[7], m));
-        // exponent reference in log2 units; a row with nothing visible yet
-        // keeps 0 as its reference
-        const float mref_new = (m == -INFINITY) ? 0.f : m * sl2;
-        const float alpha = ex2_approx(mref - mref_new);  // no reference yet -> 0
+        // Exponent reference in log2 units.  It moves to the new maximum only
+        // when that exceeds it by more than kRefSlack, or when the row had no
+        // visible key before this block: P = 2^(s - mref) stays below
+        // 2^kRefSlack, which the fp32 sums and bf16 P hold without loss, and
+        // O_t needs its rescale (TMEM round trips) only when the reference
+        // moves, which after a row's first block is rare.  O / l and
+        // LSE = mref + log2 l are the same whichever reference is used.  A row
+        // with nothing visible yet keeps 0.  (E8: no slack, 2^8 P already
+        // fills E4M3's range.)
+        constexpr float kRefSlack = E8 ? 0.f : 8.f;
+        const float cand = (m == -INFINITY) ? 0.f : m * sl2;
+        const bool move = (m_prev == -INFINITY) || (cand > mref + kRefSlack);
+        const float mref_new = move ? cand : mref;
+        const float alpha = move ? ex2_approx(mref - mref_new) : 1.f;  // no reference yet -> 0
         mref = mref_new;
         // P = 2^(scale*log2(e)*s - mref): one packed fma per pair, row sum
         // in four packed accumulators

@@ -78,15 +78,21 @@ def test_bf16_forward_window(N, w):
 
 
 def test_later_block_holds_the_max():
-    """Rows whose maximum arrives in a later key block rescale O (both column
-    halves of the row must agree on the maximum)."""
+    """The largest scores of every row sit in the last key block ("FlashAttention
+    from scratch" test recipe, as at d = 128), so every row rescales there and
+    both column halves of a row must agree on the maximum.  The 1e-2 bound on
+    O assumes |O| < 2 (bf16 output rounding); the recipe keeps it there."""
     x = h.seeded(1, 2, 640, 256, seed=3200)
     k = x["K"].float()
-    k[:, :, 500:520] *= 3.0
+    k[:, :, -100:] *= 3.0
     x["K"] = k.to(torch.bfloat16)
+    # at d = 256 the raised keys dominate more than at d = 128: V / 4 keeps
+    # |O| below 2 (the window tests' treatment of peaked rows)
+    x["V"] = (x["V"].float() * 0.25).to(torch.bfloat16)
     sc = 256 ** -0.5
     o, lse = run_fwd(x, sc, False)
     O, L = oracle.fwd(*f64(x, ("Q", "K", "V")), sc, False)
+    assert np.abs(O).max() < 2.0
     assert h.max_abs(o, O) <= h.TOL_O_BF16
     assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
 

@@ -99,11 +99,15 @@ def test_bf16_later_block_holds_the_max():
 
 def test_bf16_large_logits_stay_finite():
     """Logits with a range near 58 ("LLM Architecture Refresh [3]",
-    section 3): no overflow, no NaN."""
+    section 3): no overflow, no NaN.  Such rows are nearly one-hot, so O
+    copies rows of V; V / 4 keeps |O| below 2, where the 1e-2 bound holds
+    (bf16 output rounding alone exceeds it for |O| >= 4)."""
     N, d = 512, 64
     x = h.seeded(1, 2, N, d, seed=78, dtype="bf16")
+    x["V"] = (x["V"].float() * 0.25).to(torch.bfloat16)
     o, lse = run_fwd(x, 1.0, True)
     O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), 1.0, True)
+    assert np.abs(O).max() < 2.0
     assert h.max_abs(o, O) <= h.TOL_O_BF16
     assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
 

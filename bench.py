@@ -68,7 +68,8 @@ def measured_peaks():
 
 
 # kernel key (as in profiles/traffic.txt) -> the source file that defines it
-KERNEL_SOURCES = {"bwd_kernel": "fa_bwd_tc.cu", "fwd_kernel": "fa_fwd_tc.cu"}
+KERNEL_SOURCES = {"bwd_kernel": "fa_bwd_tc.cu", "fwd_kernel": "fa_fwd_tc.cu",
+                  "fwd256_kernel": "fa_fwd256_tc.cu"}
 
 
 def kernel_digest(kernel_key):

@@ -182,7 +182,6 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
         s, static_cast<const float*>(Q), static_cast<const float*>(K),
         static_cast<const float*>(V), static_cast<float*>(O), LSE, cs));
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
-  if (d == 256 && drop.t4 != 0) return FA_ERR_UNSUPPORTED;  // no bf16 d = 256 dropout
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TileMaps maps;
   const int BH = B * H;
@@ -325,7 +324,6 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   }
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
   if (d == 256) {  // CUDA cores: the tensor-core backward's TMEM does not fit
-    if (drop.t4 != 0) return FA_ERR_UNSUPPORTED;
     if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, nullptr, cs))) != FA_OK)
       return st;
     return from_cuda(fa::launch_bwd_simt_bf16(s, Q, K, V, dO, LSE, Dvec, dQ, dK,

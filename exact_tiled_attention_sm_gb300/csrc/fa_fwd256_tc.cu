@@ -34,6 +34,7 @@
 
 #include "fa_internal.h"
 #include "fa_sched.cuh"
+#include "fa_philox.cuh"
 #include "fa_tiles.cuh"
 
 namespace fa {
@@ -78,6 +79,7 @@ struct Params {
   float* LSE;
   float scale_log2;
   uint64_t wait_limit_ns;
+  DropSpec drop;  // DR variant only
   FwdSched sched;
 };
 
@@ -87,7 +89,9 @@ enum : uint32_t {
   SITE_S_XL, SITE_DRAIN, SITE_ALIGN, SITE_S_ODONE
 };
 
-template <bool W>
+// W: causal sliding window; DR: dropout (keep bytes drawn per 32-key half as
+// in the d <= 128 forward: two Philox calls per lane and a quad transpose).
+template <bool W, bool DR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd256_kernel(const __grid_constant__ CUtensorMap mq,
                   const __grid_constant__ CUtensorMap mk,
@@ -329,6 +333,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          // keep flags of this row for keys 64g + 32h + 4c + (0..3)
+          uint32_t kw[8];
+          if constexpr (DR) {
+            const uint32_t kp0 = (uint32_t)(j * 32 + 16 * g + 8 * h) + (uint32_t)(lane & 3);
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+              const Philox4 o = philox4x32_10(kp0 + 4 * gg, (uint32_t)row >> 2,
+                                              (uint32_t)bh, 0u, p.drop.k0, p.drop.k1);
+              uint32_t a[4] = {o.x[0], o.x[1], o.x[2], o.x[3]};
+              quad_transpose(a, lane);
+#pragma unroll
+              for (int c = 0; c < 4; ++c) kw[4 * gg + c] = keep_flags(a[c], p.drop);
+            }
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -339,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             b = ex2_approx(b);
             acc[i & 3] = fadd2(acc[i & 3], f2_pack(a, b));
             pk[i] = pack_bf16x2(a, b);
+            if constexpr (DR) pk[i] &= pair_mask(kw[i >> 1], i);
           }
           // P of keys 64g + 32h + (0..31): columns 32g + 16h .. + 15 (inside
           // the columns both halves have already read)
@@ -395,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_warp(bar(B_XL + wq), it & 1, abort_flag, lim, SITE_S_XL)) break;
       __syncwarp();
       const float lt = l + xl[(g ^ 1) * 128 + rb];
-      const float inv_l = 1.f / lt;
+      const float inv_l = (DR ? p.drop.keep_scale : 1.f) / lt;
       const bool store = row < sc.N;
       __nv_bfloat16* orow =
           p.O + ((size_t)bh * sc.N + (size_t)(store ? row : 0)) * D + 128 * g;
@@ -433,23 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <bool W>
+template <bool W, bool DR>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O, float* LSE,
                    int num_sms, uint64_t lim, cudaStream_t stream) {
   static cudaError_t attr = cudaFuncSetAttribute(
-      fwd256_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      fwd256_kernel<W, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (attr != cudaSuccess) return attr;
   Params p;
   p.O = reinterpret_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.wait_limit_ns = lim;
+  p.drop = s.drop;
   const int BH = s.B * s.H;
   FwdSched probe;
   probe.init(BH, s.N, s.causal, num_sms, s.window, 1);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window, 1);
-  fwd256_kernel<W><<<grid, kThreads, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, p);
+  fwd256_kernel<W, DR><<<grid, kThreads, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
@@ -458,9 +478,13 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O, float* LSE
 cudaError_t launch_fwd256_tc(const AttnShape& s, const TileMaps& maps, void* O,
                              float* LSE, int num_sms, uint64_t wait_limit_ns,
                              cudaStream_t stream) {
-  return s.window > 0
-             ? fwd256::launch<true>(s, maps, O, LSE, num_sms, wait_limit_ns, stream)
-             : fwd256::launch<false>(s, maps, O, LSE, num_sms, wait_limit_ns, stream);
+  const uint64_t lim = wait_limit_ns;
+  const bool w = s.window > 0;
+  if (s.drop.t4 != 0)
+    return w ? fwd256::launch<true, true>(s, maps, O, LSE, num_sms, lim, stream)
+             : fwd256::launch<false, true>(s, maps, O, LSE, num_sms, lim, stream);
+  return w ? fwd256::launch<true, false>(s, maps, O, LSE, num_sms, lim, stream)
+           : fwd256::launch<false, false>(s, maps, O, LSE, num_sms, lim, stream);
 }
 
 FA_DEFINE_STATUS_READER(read_status_fwd256_tc)

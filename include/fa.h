@@ -36,8 +36,7 @@
  *     memory): the bf16 forward runs on the tensor cores with one 128-row
  *     query block per work item; the bf16 backward runs on the CUDA cores in
  *     fp32 arithmetic (its tensor-core layout would need 768 TMEM columns);
- *     fp32 inputs run on the CUDA cores as for every d; bf16 dropout at
- *     d = 256 is FA_ERR_UNSUPPORTED.
+ *     fp32 inputs run on the CUDA cores as for every d.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  The returned status covers argument checks and the
  *     launch only; device-side failures (a bounded wait that ran out) are

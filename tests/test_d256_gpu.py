@@ -154,10 +154,46 @@ def test_f32(causal):
     assert max(errs) < 1e-5
 
 
-def test_dropout_is_unsupported_at_d256():
-    q = torch.zeros((1, 1, 16, 256), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(fa.FAError):
-        fa.fwd(q, q, q, 1.0, dropout_p=0.1, seed=1)
+@pytest.mark.parametrize("N,causal,window", [(300, False, 0), (513, True, 0), (700, True, 200)])
+def test_dropout(N, causal, window):
+    """Dropout at d = 256: the forward's keep decisions (tensor-core kernel)
+    and the backward's (CUDA cores, one Philox call per entry) are the
+    oracle's; bf16 O bound times the keep factor."""
+    x = h.seeded(1, 2, N, 256, seed=3700 + N, with_dO=True)
+    sc, p, seed = 256 ** -0.5, 0.2, 99 + N
+    q, k, v, do = (x[n].to("cuda") for n in ("Q", "K", "V", "dO"))
+    o, lse = fa.fwd(q, k, v, sc, causal, window=window, dropout_p=p, seed=seed)
+    dq, dk, dv = fa.bwd(q, k, v, o, do, lse, sc, causal, window=window, dropout_p=p,
+                        seed=seed)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    Q, K, V, dO = f64(x, ("Q", "K", "V", "dO"))
+    O, L = oracle.fwd(Q, K, V, sc, causal, window=window, dropout_p=p, seed=seed)
+    keep_factor = 256.0 / (256 - oracle.dropout_threshold(p))
+    assert h.max_abs(h.np64(o), O) <= h.TOL_O_BF16 * keep_factor
+    assert h.max_abs(h.np64(lse), L) <= h.TOL_LSE_BF16
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, causal, window=window, dropout_p=p,
+                               seed=seed)
+    check_grads((h.np64(dq), h.np64(dk), h.np64(dv)), (dQ, dK, dV))
+
+
+def test_dropout_forward_applies_the_oracle_mask():
+    """Q = K = 0 and V a shifted identity expose the d = 256 forward's keep
+    decisions bit for bit (as in the d <= 128 mask tests)."""
+    B, H, N, d, p, seed = 1, 2, 384, 256, 0.5, 7
+    z = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    got = np.zeros((B, H, N, N), bool)
+    for c0 in range(0, N, d):
+        n = min(d, N - c0)
+        v.zero_()
+        idx = torch.arange(n, device="cuda")
+        v[:, :, c0 + idx, idx] = 1
+        o, _ = fa.fwd(z, z, v, 1.0, False, dropout_p=p, seed=seed)
+        torch.cuda.synchronize()
+        got[:, :, :, c0:c0 + n] = (o[..., :n] != 0).cpu().numpy()
+    ref = oracle.dropout_keep(B, H, N, p, seed).astype(bool)
+    assert np.array_equal(got, ref), int((got != ref).sum())
 
 
 def test_repeated_runs_are_bit_identical():

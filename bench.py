@@ -162,22 +162,33 @@ def dist_setup():
     return world, rank, local
 
 
-def barrier(world):
+def barrier(world, device="cuda"):
+    """Device work done and every rank here (device "cpu": host-only ranks,
+    as in the gloo tests of this logic)."""
     import torch
-    torch.cuda.synchronize()
+    if device == "cuda":
+        torch.cuda.synchronize()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """The largest of the ranks' values of x (a time: the job is as slow as
+    its slowest replica)."""
     import torch
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world, flops_per_rank, ms):
+    """Whole-job throughput: every rank processes its own replica of the
+    workload (weak scaling), the job takes the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------ profile
@@ -361,7 +372,7 @@ def run_ours(args):
             ms = max_over_ranks(a.elapsed_time(b), world) / reps
             fl = attn_flops(wf.B, wf.H, wf.N, wf.d, c, "fwd")
             key = f"{name}{'_causal' if c else ''}"
-            fwd_results[key] = {"tflops": round(world * fl / (ms * 1e-3) / 1e12, 1),
+            fwd_results[key] = {"tflops": round(job_tflops(world, fl, ms), 1),
                                 "ms": round(ms, 4), "launches": reps}
             if name == "gpt2_medium_fwd":  # 48 MiB of inputs: L2 stays warm
                 fwd_results[key]["l2"] = "warm (inputs smaller than L2; launch-bound shape)"
@@ -411,7 +422,7 @@ def run_ours(args):
         ms, nl = time_variant(name, passes, True, win=win)
         fl = window_flops(wf.B, wf.H, wf.N, wf.d, win, passes)
         window_results[f"{name}_w{win}_{passes.replace('+', '_')}"] = {
-            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "tflops": round(job_tflops(world, fl, ms), 1), "ms": round(ms, 4),
             "window": win, "launches": nl}
         launches += nl
 
@@ -424,7 +435,7 @@ def run_ours(args):
         ms, nl = time_variant(name, passes, causal_v, drop=0.1, seed=1234)
         fl = attn_flops(wf.B, wf.H, wf.N, wf.d, causal_v, passes)
         dropout_results[f"{name}{'_causal' if causal_v else ''}_p0.1_{passes.replace('+', '_')}"] = {
-            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "tflops": round(job_tflops(world, fl, ms), 1), "ms": round(ms, 4),
             "dropout_p": 0.1, "launches": nl}
         launches += nl
     # --- the 8-bit forward (E4M3 inputs with per-tensor factors): the 4096-
@@ -453,7 +464,7 @@ def run_ours(args):
             ms = max_over_ranks(a.elapsed_time(b), world) / reps
             fl = attn_flops(wf.B, wf.H, wf.N, wf.d, c, "fwd")
             fp8_results[f"{name}{'_causal' if c else ''}_e4m3"] = {
-                "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+                "tflops": round(job_tflops(world, fl, ms), 1), "ms": round(ms, 4),
                 "launches": reps}
             launches += reps
         del q8, k8, v8, of, lf
@@ -467,7 +478,7 @@ def run_ours(args):
         ms, nl = time_variant(name, passes, causal_v)
         fl = attn_flops(wf.B, wf.H, wf.N, wf.d, causal_v, passes)
         d256_results[f"{name}{'_causal' if causal_v else ''}_{passes.replace('+', '_')}"] = {
-            "tflops": round(world * fl / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+            "tflops": round(job_tflops(world, fl, ms), 1), "ms": round(ms, 4),
             "launches": nl}
         launches += nl
     clocks = sampler.stop()
@@ -480,7 +491,7 @@ def run_ours(args):
     peak, peak_sustained, peak_src = measured_peaks()
     step_flops = attn_flops(B, H, N, d, causal, "fwd+bwd")
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(world, step_flops, ms_per_step)
     bwd_flops = step_flops - attn_flops(B, H, N, d, causal, "fwd")
     bwd_tflops = bwd_flops / (bwd_ms * 1e-3) / 1e12
     fwd_tflops = attn_flops(B, H, N, d, causal, "fwd") / (fwd_ms * 1e-3) / 1e12
@@ -534,7 +545,7 @@ def run_ours(args):
         "fp8": fp8_results,
         "d256": d256_results,
         "fp8_peak_note": "8-bit dense peak taken as 2 x the measured bf16 burst peak (the nominal 4.5 / 2.25 PFLOP/s ratio)",
-        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(job_tflops(world, step_flops, e2e_ms), 2),
                 "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

@@ -21,9 +21,11 @@
 //
 // Per key block j (queries outer, "LLM Architecture Refresh [3]", section 4):
 //   MMA   S_j = Q K_j^T into S buffer j%2 (issued two blocks ahead)
-//   softmax: max of both halves, alpha, P = 2^(S - m) as bf16 over the
-//         block's first 64 columns, l, O *= alpha when a row's max moved
-//         (after the previous P V product has completed)
+//   softmax: max of both halves, the exponent reference (it follows the
+//         max only when the max has risen past it by more than 8, log2),
+//         alpha, P = 2^(S - reference) as bf16 over the block's first 64
+//         columns, l, O *= alpha when a row's reference moved (after the
+//         previous P V product has completed)
 //   MMA   O += P_j V_j (P from TMEM, V MN-major, N = 256)
 // and O = O / l, LSE = (m + log2 l) ln 2 once at the end.
 //

@@ -14,9 +14,11 @@
 //   TMA    K_j, V_j  HBM -> shared memory (128-byte swizzled, 2-4 stage ring)
 //   MMA    S_t = Q_t K_j^T             (tcgen05, fp32 accumulator in TMEM)
 //   softmax t: S_t -> registers, scale by scale*log2(e), mask the diagonal /
-//          ragged block, m_new = max(m, rowmax), alpha = 2^(m - m_new),
-//          P = 2^(S - m_new) (bf16, written back over S_t in TMEM),
-//          l = alpha*l + rowsum(P), O_t *= alpha when the max moved
+//          ragged block, m = max(m, rowmax); the exponent reference r
+//          follows m only when m has risen past it by more than 8 (log2),
+//          alpha = 2^(r_old - r), P = 2^(S - r) < 2^8 (bf16, written back
+//          over S_t in TMEM), l = alpha*l + rowsum(P), O_t *= alpha when a
+//          row's reference moved (rare after its first block)
 //   MMA    O_t += P_t V_j              (A operand straight from TMEM)
 // and after the last block O = O_t / l, LSE = (m + log2 l) * ln 2 (the
 // division deferred to the end, "FlashAttention from scratch", Step 3).

@@ -8,8 +8,10 @@
  *     O = softmax(scale * Q K^T) V,        LSE_r = m_r + ln(l_r),
  *
  * tile by tile with an online softmax: a running row max m and a running row
- * sum l rescale the partial output whenever a later key/value block raises
- * the max, and the division by l happens once at the end ("Flash Attention,
+ * sum l rescale the partial output when a later key/value block raises the
+ * max (the forward keeps its exponent reference until the max has risen past
+ * it by a factor 2^8, which leaves O / l and LSE unchanged and makes the
+ * rescale rare), and the division by l happens once at the end ("Flash Attention,
  * From First Principles", sections "Online softmax -- the game" through "The
  * scaffold"; "LLM Architecture Refresh [3]", section 4).  The N x N score
  * matrix never reaches device memory.  With causal != 0, key k is visible to

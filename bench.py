@@ -357,6 +357,11 @@ def run_ours(args):
         qf, kf, vf = (xf[n].cuda() for n in ("Q", "K", "V"))
         of = torch.empty_like(qf)
         lf = torch.empty((wf.B, wf.H, wf.N), dtype=torch.float32, device="cuda")
+        # inputs smaller than L2 (the GPT-2-shaped workload, 48 MiB): each
+        # timed call is preceded by a 256 MiB write that evicts them, outside
+        # its own pair of events
+        small = (3 * qf.numel() * qf.element_size()) < (129 << 20)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if small else None
         for c in causal_list:
             reps = max(5, args.steps // 2)
             for _ in range(3):
@@ -372,12 +377,27 @@ def run_ours(args):
             ms = max_over_ranks(a.elapsed_time(b), world) / reps
             fl = attn_flops(wf.B, wf.H, wf.N, wf.d, c, "fwd")
             key = f"{name}{'_causal' if c else ''}"
+            launches += reps
+            if small:
+                warm_ms = ms
+                evs = [(torch.cuda.Event(enable_timing=True),
+                        torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+                barrier(world)
+                for i in range(reps):
+                    flush.fill_(i & 0xFF)
+                    evs[i][0].record(stream)
+                    fa.fwd(qf, kf, vf, wf.scale, c, out=of, lse=lf)
+                    evs[i][1].record(stream)
+                barrier(world)
+                ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in evs), world) / reps
+                launches += reps
             fwd_results[key] = {"tflops": round(job_tflops(world, fl, ms), 1),
                                 "ms": round(ms, 4), "launches": reps}
-            if name == "gpt2_medium_fwd":  # 48 MiB of inputs: L2 stays warm
-                fwd_results[key]["l2"] = "warm (inputs smaller than L2; launch-bound shape)"
-            launches += reps
-        del qf, kf, vf, of, lf
+            if small:
+                fwd_results[key]["l2"] = ("flushed: a 256 MiB write before each call, "
+                                          "outside its timed events")
+                fwd_results[key]["tflops_warm_l2"] = round(job_tflops(world, fl, warm_ms), 1)
+        del qf, kf, vf, of, lf, flush
 
     def time_variant(name, passes, causal_v, win=0, drop=0.0, seed=0):
         """Device time of one fa_fwd (+ fa_bwd) call pair of a mask or dropout

@@ -185,6 +185,14 @@ def max_over_ranks(x, world, device="cuda"):
     return float(t.item())
 
 
+def bench_config(w, world):
+    """The `config` of the bench line, identical in both arms."""
+    return {"workload": "train_fwd_bwd: B=8 H=16 N=2048 d=128 bf16 causal, fa_fwd + fa_bwd",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True, "scale": w.scale,
+            "parallelism": f"replicas x{world} (heads independent; no collective)",
+            "l2": "no flush: inputs larger than L2 (Q, K, V, dO, O are 64 MiB each; 320 MiB read per step)"}
+
+
 def job_tflops(world, flops_per_rank, ms):
     """Whole-job throughput: every rank processes its own replica of the
     workload (weak scaling), the job takes the slowest rank's time."""
@@ -232,6 +240,58 @@ def run_profile(args):
     return {"profile": args.workload, "causal": causal, "steps": args.steps,
             "warmup": args.warmup, "window": args.window, "dropout": args.dropout,
             "fp8": bool(args.fp8)}
+
+
+# ------------------------------------------------------------------ balance
+BALANCE_CASES = (("llama3_8b_fwd", True, "fwd"), ("llama3_8b_fwd", False, "fwd"),
+                 ("gpt2_medium_fwd", True, "fwd"), ("gpt2_medium_fwd", False, "fwd"),
+                 ("long_ctx_32k", True, "fwd"), ("train_fwd_bwd", True, "fwd"),
+                 ("train_fwd_bwd", True, "bwd"))
+
+
+def run_balance(args):
+    """How evenly the schedulers spread the work: the trace build of the
+    library (libfa_trace.so, built on demand) records each CTA's start and
+    end; for every case, three traced launches after three warm-up launches,
+    summarised per launch (exact_tiled_attention_sm_gb300.trace.summarize).
+    Inputs are drawn on the device (no parity check here)."""
+    import torch
+    import exact_tiled_attention_sm_gb300 as fa
+    from exact_tiled_attention_sm_gb300 import _build, inputs, trace
+    fa.use_library(_build.build(trace=True))
+    L = fa.lib()
+    torch.cuda.set_device(0)
+    out = {}
+    for name, causal, which in BALANCE_CASES:
+        w = inputs.WORKLOADS[name]
+        x = inputs.seeded_inputs_cuda(w.B, w.H, w.N, w.d, w.seed, with_dO=(which == "bwd"))
+        q, k, v = x["Q"], x["K"], x["V"]
+        o, lse = fa.fwd(q, k, v, w.scale, causal)
+        if which == "bwd":
+            do = x["dO"]
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            ws = fa.workspace(w.B, w.H, w.N, w.d)
+
+        def call():
+            if which == "bwd":
+                fa.bwd(q, k, v, o, do, lse, w.scale, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+            else:
+                fa.fwd(q, k, v, w.scale, causal, out=o, lse=lse)
+
+        runs = []
+        for rep in range(6):
+            call()
+            marks = trace.read(L, "fwd256" if (which == "fwd" and w.d == 256) else which)
+            if rep >= 3:
+                runs.append(trace.summarize(marks))
+        st = fa.last_device_status()
+        if st != fa.FA_OK:
+            raise SystemExit(f"device status: {fa.status_string(st)}")
+        out[f"{name}{'_causal' if causal else ''}_{which}"] = {
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal, "launches": runs}
+        del x, q, k, v, o, lse
+    return {"balance": out, "note": "per-CTA global-timer marks from libfa_trace.so "
+            "(FA_CTA_TRACE build); times in microseconds relative to the launch's first CTA start"}
 
 
 # --------------------------------------------------------------------- ours
@@ -334,7 +394,10 @@ def run_ours(args):
         stream.wait_event(ev_out[(k0 + nsteps - 1) & 1])
         stream.wait_event(ev_out[(k0 + nsteps - 2) & 1])
 
-    e2e_steps = max(3, args.steps // 4)
+    # at least 20 timed steps: the pipeline's fill (the first step's copy-in)
+    # and drain (the last step's copy-out) are not overlapped, and over a
+    # handful of steps they dominate the per-step figure
+    e2e_steps = max(20, args.steps)
     e2e_run(2, 0)
     torch.cuda.synchronize()
     barrier(world)
@@ -533,10 +596,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic: seeded iid N(0,1) bf16 tensors of the workload's shape",
-        "config": {"workload": "train_fwd_bwd: B=8 H=16 N=2048 d=128 bf16 causal, fa_fwd + fa_bwd",
-                   "B": B, "H": H, "N": N, "d": d, "causal": True, "scale": sc,
-                   "parallelism": f"replicas x{world} (heads independent; no collective)",
-                   "l2": "no flush: inputs larger than L2 (Q, K, V, dO, O are 64 MiB each; 320 MiB read per step)"},
+        "config": bench_config(w, world),
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {
             "bound": "tensor",
@@ -634,8 +694,7 @@ def run_reference(args):
         "ms_per_step": round(1e3 * tot_s / args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic: seeded iid N(0,1), rounded to bf16, widened to fp64",
-        "config": {"workload": "train_fwd_bwd: B=8 H=16 N=2048 d=128 bf16 causal, fa_fwd + fa_bwd",
-                   "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True},
+        "config": bench_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s",
@@ -659,9 +718,13 @@ def main():
     ap.add_argument("--window", type=int, default=0, help="profile: sliding window")
     ap.add_argument("--dropout", type=float, default=0.0, help="profile: dropout p")
     ap.add_argument("--fp8", action="store_true", help="profile: the 8-bit forward")
+    ap.add_argument("--balance", action="store_true",
+                    help="per-CTA balance of the schedulers (trace build)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.profile:
+    if args.balance:
+        line = run_balance(args)
+    elif args.profile:
         line = run_profile(args)
     elif args.impl == "reference":
         line = run_reference(args)

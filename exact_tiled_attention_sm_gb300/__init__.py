@@ -34,6 +34,17 @@ class FAError(RuntimeError):
         super().__init__(f"{what}: {status_string(status)} (status {status})")
 
 
+def use_library(path):
+    """Makes every later call go to the library at ``path`` instead of
+    libfa.so; only before the first call.  bench.py --balance uses it to load
+    the trace build (libfa_trace.so: the same kernels, recording per-CTA
+    start and end times)."""
+    global LIB_PATH
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded")
+    LIB_PATH = path
+
+
 def lib():
     """Loads libfa.so (raising if it has not been built)."""
     global _lib

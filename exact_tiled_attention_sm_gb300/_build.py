@@ -3,6 +3,11 @@
 One object per translation unit, compiled in parallel, then one nvcc link with
 the static CUDA runtime (the library loads without a GPU driver present, and
 fetches the driver's tensor-map encoder at run time).
+
+build(trace=True) builds libfa_trace.so instead: the same sources with
+FA_CTA_TRACE defined, whose persistent kernels also record per-CTA start and
+end times (csrc/fa_trace.cuh) for measuring the schedulers' balance.  It is a
+measurement build, loaded only by `bench.py --balance`.
 """
 import os
 import subprocess
@@ -15,6 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa.so")
+TRACE_LIB = os.path.join(PKG, "libfa_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -37,16 +43,19 @@ def _deps_mtime():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force=False, verbose=False):
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, trace=False):
+    lib_path = TRACE_LIB if trace else LIB
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _deps_mtime():
+        return lib_path
+    objdir = os.path.join(BUILD, "trace") if trace else BUILD
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     srcs = sources()
+    extra = ["-DFA_CTA_TRACE"] if trace else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,15 +68,16 @@ def build(force=False, verbose=False):
     if verbose:
         for _, err in results:
             sys.stderr.write(err)
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp,
            *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                trace="--trace" in sys.argv))

@@ -48,9 +48,12 @@
 #include "fa_philox.cuh"
 #include "fa_sched.cuh"
 #include "fa_tiles.cuh"
+#include "fa_trace.cuh"
 
 namespace fa {
 namespace bwdtc {
+
+FA_TRACE_DEFINE(g_cta_trace, fa_cta_trace_bwd)
 
 template <int D>
 struct Cfg {
@@ -340,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 0);
   const uint32_t tmem = *tmem_slot;
   const int nw = sc.n_waves();
 
@@ -720,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 1);
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 

@@ -38,9 +38,12 @@
 #include "fa_sched.cuh"
 #include "fa_philox.cuh"
 #include "fa_tiles.cuh"
+#include "fa_trace.cuh"
 
 namespace fa {
 namespace fwd256 {
+
+FA_TRACE_DEFINE(g_cta_trace, fa_cta_trace_fwd256)
 
 constexpr int D = 256;
 constexpr int CH = D / 64;
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 0);
   const uint32_t tmem = *tmem_slot;
   const int nw = sc.n_waves();
 
@@ -328,7 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cand = (m == -INFINITY) ? 0.f : m * sl2;
         const bool move = (m_prev == -INFINITY) || (cand > mref + 8.f);
         const float mref_new = move ? cand : mref;
-        const float alpha = move ? ex2_approx(mref - mref_new) : 1.f;
+        // a row that has seen no key yet has nothing to rescale: alpha = 0
+        // (under the window its first visible keys may come in a later block,
+        // where 2^(0 - cand) from the placeholder reference could overflow)
+        const float alpha =
+            !move ? 1.f : ((W && m_prev == -INFINITY) ? 0.f : ex2_approx(mref - mref_new));
         mref = mref_new;
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
         const uint64_t nm2 = f2_pack(-mref_new, -mref_new);
@@ -451,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 1);
   if (warp == kMmaWarp) tmem_dealloc(tmem, TMEM_COLS);
 }
 

@@ -48,9 +48,12 @@
 #include "fa_philox.cuh"
 #include "fa_sched.cuh"
 #include "fa_tiles.cuh"
+#include "fa_trace.cuh"
 
 namespace fa {
 namespace fwdtc {
+
+FA_TRACE_DEFINE(g_cta_trace, fa_cta_trace_fwd)
 
 template <int D, bool E8 = false>
 struct Cfg {
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 0);
   const uint32_t tmem = *tmem_slot;
 
   auto sQ = [&](int t) { return sb + C::OFF_Q + (uint32_t)t * C::TILE_BYTES; };
@@ -460,7 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float cand = (m == -INFINITY) ? 0.f : m * sl2;
         const bool move = (m_prev == -INFINITY) || (cand > mref + kRefSlack);
         const float mref_new = move ? cand : mref;
-        const float alpha = move ? ex2_approx(mref - mref_new) : 1.f;  // no reference yet -> 0
+        // alpha rescales what the row has accumulated so far.  A row that has
+        // seen no key yet has nothing (l = 0, O_t = 0), so alpha = 0; under
+        // the window this also covers a row whose first visible keys come in
+        // a later block, where mref still holds the placeholder 0 and
+        // 2^(0 - cand) would overflow for very negative scores (inf * 0).
+        const float alpha =
+            !move ? 1.f : ((W && m_prev == -INFINITY) ? 0.f : ex2_approx(mref - mref_new));
         mref = mref_new;
         // P = 2^(scale*log2(e)*s - mref): one packed fma per pair, row sum
         // in four packed accumulators
@@ -609,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  FA_TRACE_MARK(g_cta_trace, 1);
   if (warp == kMmaWarp) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 

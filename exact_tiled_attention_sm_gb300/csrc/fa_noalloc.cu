@@ -1,8 +1,11 @@
 // fa_noalloc.cu -- fa_bwd_noalloc: the backward pass with a library-owned
 // scratch array instead of a caller workspace, for callers that have input
 // and output buffers but no way to allocate device memory (see include/fa.h).
-// It reserves FA_BWD_NOALLOC_SCRATCH_BYTES once per device that loads this
-// code and then runs exactly fa_bwd on it.
+// The array is a file-scope __device__ variable.  CUDA reserves it on a
+// device when this module is loaded there; with lazy module loading (CUDA's
+// default) that is the first cudaGetSymbolAddress of it on that device, made
+// by the first fa_bwd_noalloc call there, which can therefore take device
+// memory and synchronise.  Later calls run exactly fa_bwd on the array.
 #include <cstdint>
 #include <mutex>
 
@@ -45,7 +48,7 @@ extern "C" __attribute__((visibility("default"))) fa_status fa_bwd_noalloc(
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {  // first call on this device: resolve, keep
+    if (!g_scratch_ptr[dev]) {  // first call on this device: load, resolve, keep
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p)
         return FA_ERR_CUDA;

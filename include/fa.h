@@ -178,8 +178,10 @@ fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O,
                      float v_descale, void* stream);
 
 /* Size of the device scratch array that fa_bwd_noalloc uses in place of a
- * caller workspace: 64 MiB, statically reserved on every GPU that loads the
- * library (the reservation lasts until the process exits). */
+ * caller workspace: 64 MiB of static device memory, reserved on a GPU when
+ * the code holding it is loaded there (with CUDA's default lazy loading: at
+ * the first fa_bwd_noalloc call on that GPU) and held until the process
+ * exits. */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
 
 /* The backward pass for callers that cannot allocate device memory.  Some
@@ -196,9 +198,16 @@ fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O,
  *     with FA_ERR_INVALID_ARG before anything is launched (for d = 128 that
  *     is B*H*N above about 130,000 rows: 32 heads of 2048 fit, 32 of 4096 do
  *     not).  Other argument errors are those of fa_bwd.
- *   - The first call on a device looks up the array's device address on
- *     that device (cudaGetSymbolAddress, with that device current) and
- *     keeps it; make that first call before any stream capture.
+ *   - The first call on a device is its set-up: it looks up the array's
+ *     device address there (cudaGetSymbolAddress, with that device current)
+ *     and keeps it.  That lookup loads the library's device code on that
+ *     device if it is not loaded yet, which reserves the array: the one
+ *     moment this entry point takes device memory, and it can synchronise.
+ *     Make that first call before any stream capture and outside
+ *     latency-critical loops (a warm-up call on each device does it).
+ *   - The kept address belongs to the device's current context: after
+ *     cudaDeviceReset on a device it is no longer valid, and this entry
+ *     point must not be called there again in the same process.
  *   - All calls in the process share the one array and it keeps the last
  *     call's contents; the backward clears what must start at zero itself.
  *     Calls that overlap on the GPU (different streams, or several host

@@ -52,3 +52,15 @@ def np64(t):
 
 def seeded(B, H, N, d, seed, dtype="bf16", with_dO=False):
     return inputs.seeded_inputs(B, H, N, d, seed, dtype, with_dO)
+
+
+def late_first_key_inputs(N, d, seed):
+    """Window inputs whose scaled scores all lie near -128 (natural-log
+    units; about -185 in log2 units): Q near +1 and K near -1 in every
+    coordinate, scale 128/d.  V is scaled by 1/4, since window rows are
+    peaked.  Returns (inputs, scale)."""
+    x = seeded(1, 2, N, d, seed, dtype="bf16")
+    x["Q"] = (1.0 + 0.25 * x["Q"].float()).to(torch.bfloat16)
+    x["K"] = (-1.0 - 0.25 * x["K"].float()).to(torch.bfloat16)
+    x["V"] = (x["V"].float() * 0.25).to(torch.bfloat16)
+    return x, 128.0 / d

@@ -77,6 +77,19 @@ def test_bf16_forward_window(N, w):
     assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
 
 
+@pytest.mark.parametrize("N,w", [(300, 16), (520, 100)])
+def test_window_row_whose_first_visible_key_is_in_a_later_block(N, w):
+    """As the d <= 128 test of the same name: rows that see nothing in the
+    first key block of their window, with all scaled scores near -128, so
+    that rebasing from the placeholder reference would overflow."""
+    x, sc = h.late_first_key_inputs(N, 256, seed=3700 + N + w)
+    o, lse = run_fwd(x, sc, True, window=w)
+    O, L = oracle.fwd(*f64(x, ("Q", "K", "V")), sc, window=w)
+    assert L.max() < -40.0
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
 def test_later_block_holds_the_max():
     """The largest scores of every row sit in the last key block ("FlashAttention
     from scratch" test recipe, as at d = 128), so every row rescales there and

@@ -173,6 +173,67 @@ def test_f32_window_small(N, w):
     assert h.max_abs(lse, L) <= h.TOL_F32
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N,w", [(300, 16), (640, 40), (520, 100)])
+def test_window_row_whose_first_visible_key_is_in_a_later_block(N, w, d):
+    """Under the window a row of query block q may see nothing in the first
+    key block the block visits (rows 128q + w .. of block q see no key of
+    block kv_lo(q)), so its first visible scores arrive in the next block
+    while the running reference is still the placeholder.  With all scaled
+    scores near -128 (times log2(e) below -128), rebasing from that
+    placeholder would overflow; O and LSE must match the oracle."""
+    x, sc = h.late_first_key_inputs(N, d, seed=700 + N + w + d)
+    o, lse = run_fwd(x, sc, True, window=w)
+    O, L = oracle.fwd(*(inputs.to_f64(x[n]) for n in ("Q", "K", "V")), sc, window=w)
+    assert L.max() < -40.0
+    assert h.max_abs(o, O) <= h.TOL_O_BF16
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
+def bf16_half_ulp(x):
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|."""
+    m, e = np.frexp(np.abs(np.asarray(x, dtype=np.float64)))  # |x| = m 2^e, m in [0.5, 1)
+    return np.where(m > 0, np.ldexp(1.0, e - 9), 0.0)
+
+
+def bf16_output_bound(Q, K, V, scale, causal):
+    """Element-wise error bound of the bf16 forward, from its arithmetic:
+    P is rounded to bf16 before the P V product (relative error <= 2^-8 per
+    weight, and the largest weight is not exactly 1 since the exponent
+    reference may trail the row maximum), while l sums the unrounded values;
+    then O is rounded to bf16 (half an ulp).  With p the exact probabilities,
+      |O - O_ref| <= (2^-8 + 2e-4) sum_k p_k |v_k|
+                     + half_ulp(|O_ref| + 2^-8 sum_k p_k |v_k|) + 1e-5,
+    the 2e-4 and 1e-5 covering the fp32 score and product sums and exp2.
+    sum_k p_k |v_k| is the oracle's forward with |V| as the values."""
+    O, L = oracle.fwd(Q, K, V, scale, causal)
+    A, _ = oracle.fwd(Q, K, np.abs(V), scale, causal)
+    bound = (2.0 ** -8 + 2e-4) * A + bf16_half_ulp(np.abs(O) + 2.0 ** -8 * A) + 1e-5
+    return O, L, bound
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_peaked_rows_within_the_rounding_bound(d, causal):
+    """Nearly one-hot rows (scale 1 on N(0,1) inputs: score spread about
+    sqrt(d)) with |V| in [2, 8), so that O copies value rows of that size:
+    the rows where the forward's rescale slack can matter.  Every element is
+    held to the bound its arithmetic gives (bf16_output_bound), and most of
+    them have |O| >= 2."""
+    N = 700
+    x = h.seeded(1, 2, N, d, seed=880 + d + causal, dtype="bf16")
+    v = x["V"].float()
+    x["V"] = (torch.sign(v) * (2.0 + 5.9 * torch.rand(v.shape, generator=torch.Generator().manual_seed(881))))
+    x["V"] = x["V"].to(torch.bfloat16)
+    o, lse = run_fwd(x, 1.0, causal)
+    Q, K, V = (inputs.to_f64(x[n]) for n in ("Q", "K", "V"))
+    O, L, bound = bf16_output_bound(Q, K, V, 1.0, causal)
+    assert np.mean(np.abs(O) >= 2.0) > 0.5
+    err = np.abs(o - O)
+    assert np.all(err <= bound), float(np.max(err - bound))
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
 def test_window_covering_the_sequence_is_the_causal_forward():
     x = h.seeded(2, 3, 700, 128, seed=9, dtype="bf16")
     oc, lc = run_fwd(x, 0.09, True)

@@ -68,12 +68,14 @@ fa_status get_encoder() {
   return FA_OK;
 }
 
-// [B*H, N, d] bf16 tensor; boxes of 64 columns x 128 rows x 1 head, 128-byte
-// swizzle, out-of-range rows read as zero.
-fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+// [B*H, N, d] bf16 tensor; boxes of 64 columns x `rows` rows (128, or 64 for
+// the d = 256 backward's query blocks) x 1 head, 128-byte swizzle,
+// out-of-range rows read as zero.
+fa_status make_map(CUtensorMap* m, const void* base, int BH, int N, int d,
+                   int rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void*>(base), dims, strides, box, estr,
@@ -323,15 +325,21 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
         static_cast<float*>(dV), cs));
   }
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
-  if (d == 256) {  // CUDA cores: the tensor-core backward's TMEM does not fit
-    if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, nullptr, cs))) != FA_OK)
-      return st;
-    return from_cuda(fa::launch_bwd_simt_bf16(s, Q, K, V, dO, LSE, Dvec, dQ, dK,
-                                              dV, cs));
-  }
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TileMaps maps;
   const int BH = B * H;
+  if (d == 256) {  // one half of d per work item, 64-query blocks
+    if ((st = make_map(&maps.q, Q, BH, N, d, 64)) != FA_OK) return st;
+    if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
+    if ((st = make_map(&maps.dO, dO, BH, N, d, 64)) != FA_OK) return st;
+    if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, dQacc, cs))) != FA_OK)
+      return st;
+    if ((st = from_cuda(fa::launch_bwd256_tc(s, maps, LSE, Dvec, V, dQacc, dK, dV,
+                                             info.num_sms, fa::kWaitLimitNs, cs))) !=
+        FA_OK)
+      return st;
+    return from_cuda(fa::launch_dq_convert(s, dQacc, dQ, cs));
+  }
   if ((st = make_map(&maps.q, Q, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
@@ -386,9 +394,10 @@ FA_API fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V,
 
 FA_API fa_status fa_last_device_status(void* stream) {
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const unsigned int words[4] = {fa::read_status_fwd_tc(cs),
+  const unsigned int words[5] = {fa::read_status_fwd_tc(cs),
                                  fa::read_status_fwd256_tc(cs),
                                  fa::read_status_bwd_tc(cs),
+                                 fa::read_status_bwd256_tc(cs),
                                  fa::read_status_simt(cs)};
   fa_status out = FA_OK;
   for (unsigned int w : words) {

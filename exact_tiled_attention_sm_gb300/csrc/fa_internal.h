@@ -56,6 +56,15 @@ cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
                           uint64_t wait_limit_ns, cudaStream_t stream);
 unsigned int read_status_bwd_tc(cudaStream_t stream);
 
+// fa_bwd256_tc.cu -- bf16 backward for d = 256 on tcgen05/TMEM.  maps.q and
+// maps.dO must have 64-row boxes (64 queries per block), maps.k 128-row ones;
+// V is read directly (into TMEM); dQacc is the fp32 accumulator, zeroed.
+cudaError_t launch_bwd256_tc(const AttnShape& s, const TileMaps& maps,
+                             const float* LSE, const float* Dvec, const void* V,
+                             float* dQacc, void* dK, void* dV, int num_sms,
+                             uint64_t wait_limit_ns, cudaStream_t stream);
+unsigned int read_status_bwd256_tc(cudaStream_t stream);
+
 // fa_simt.cu -- fp32 forward/backward on the CUDA cores, and the backward's
 // pre/post passes for both dtypes.
 cudaError_t launch_fwd_f32(const AttnShape& s, const float* Q, const float* K,
@@ -65,12 +74,6 @@ cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
                            const float* V, const float* dO, const float* LSE,
                            const float* Dvec, float* dQ, float* dK, float* dV,
                            cudaStream_t stream);
-// bf16 backward on the CUDA cores for d = 256 (fp32 arithmetic), where the
-// tensor-core backward's TMEM layout does not fit.
-cudaError_t launch_bwd_simt_bf16(const AttnShape& s, const void* Q, const void* K,
-                                 const void* V, const void* dO, const float* LSE,
-                                 const float* Dvec, void* dQ, void* dK, void* dV,
-                                 cudaStream_t stream);
 // D = rowsum(dO * O) (fp32), and dQacc zeroed when non-null.
 cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
                            int is_bf16, float* Dvec, float* dQacc,

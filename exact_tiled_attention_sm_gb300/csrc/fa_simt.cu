@@ -415,17 +415,6 @@ cudaError_t launch_bwd_f32(const AttnShape& s, const float* Q, const float* K,
   return bwd_f32_launch<128>(s, Q, K, V, dO, LSE, Dvec, dQ, dK, dV, stream);
 }
 
-cudaError_t launch_bwd_simt_bf16(const AttnShape& s, const void* Q, const void* K,
-                                 const void* V, const void* dO, const float* LSE,
-                                 const float* Dvec, void* dQ, void* dK, void* dV,
-                                 cudaStream_t stream) {
-  using B = __nv_bfloat16;
-  return bwd_f32_launch<256>(s, static_cast<const B*>(Q), static_cast<const B*>(K),
-                             static_cast<const B*>(V), static_cast<const B*>(dO),
-                             LSE, Dvec, static_cast<B*>(dQ), static_cast<B*>(dK),
-                             static_cast<B*>(dV), stream);
-}
-
 cudaError_t launch_bwd_pre(const AttnShape& s, const void* O, const void* dO,
                            int is_bf16, float* Dvec, float* dQacc,
                            cudaStream_t stream) {

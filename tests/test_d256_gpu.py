@@ -1,7 +1,8 @@
 """Head dimension 256 against the fp64 oracle: the tensor-core bf16 forward
-(one query block per work item, S double-buffered in TMEM), the CUDA-core
-bf16 backward, and the fp32 path, with the library's tolerances (bf16 O
-<= 1e-2, LSE <= 1e-3, gradients relative L2 <= 1e-2, fp32 <= 1e-5)."""
+(one query block per work item, S double-buffered in TMEM), the tensor-core
+bf16 backward (one half of d per work item, 64-query blocks, V in TMEM), and
+the fp32 path, with the library's tolerances (bf16 O <= 1e-2, LSE <= 1e-3,
+gradients relative L2 <= 1e-2, fp32 <= 1e-5)."""
 import numpy as np
 import pytest
 import torch
@@ -122,7 +123,7 @@ def test_bf16_forward_full_size_sampled(causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [7, 129, 300])
+@pytest.mark.parametrize("N", [1, 7, 63, 64, 65, 127, 128, 129, 255, 300, 513])
 def test_bf16_backward_small(N, causal):
     x = h.seeded(1, 2, N, 256, seed=3300 + N, with_dO=True)
     sc = 256 ** -0.5
@@ -131,12 +132,34 @@ def test_bf16_backward_small(N, causal):
     check_grads(got, (dQ, dK, dV))
 
 
-def test_bf16_backward_window():
-    x = h.seeded(1, 2, 500, 256, seed=3400, with_dO=True)
+@pytest.mark.parametrize("N,w", [(500, 150), (300, 1), (300, 64), (513, 129), (700, 300)])
+def test_bf16_backward_window(N, w):
+    x = h.seeded(1, 2, N, 256, seed=3400 + N + w, with_dO=True)
     sc = 256 ** -0.5
-    got = run_fwd_bwd(x, sc, True, window=150)
-    dQ, dK, dV, _ = oracle.bwd(*f64(x, ("Q", "K", "V", "dO")), sc, True, window=150)
+    got = run_fwd_bwd(x, sc, True, window=w)
+    dQ, dK, dV, _ = oracle.bwd(*f64(x, ("Q", "K", "V", "dO")), sc, True, window=w)
     check_grads(got, (dQ, dK, dV))
+
+
+def test_bf16_backward_multi_head_batch():
+    """Several heads and batches (items of different heads and both halves
+    of d interleaved on the CTAs), ragged N."""
+    x = h.seeded(2, 3, 390, 256, seed=3450, with_dO=True)
+    sc = 256 ** -0.5
+    got = run_fwd_bwd(x, sc, True)
+    dQ, dK, dV, _ = oracle.bwd(*f64(x, ("Q", "K", "V", "dO")), sc, True)
+    check_grads(got, (dQ, dK, dV))
+
+
+def test_bf16_backward_dk_dv_repeat_bit_identically():
+    """dK and dV accumulate on chip without atomics: any difference between
+    two runs is a race.  (dQ is summed with atomics, so only its values are
+    compared, within the gradient tolerance.)"""
+    x = h.seeded(2, 8, 1000, 256, seed=3460, with_dO=True)
+    a = run_fwd_bwd(x, 0.0625, True)
+    b = run_fwd_bwd(x, 0.0625, True)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert h.rel_l2(a[0], b[0]) < 1e-3
 
 
 def test_training_shape_sampled_heads():
@@ -169,8 +192,8 @@ def test_f32(causal):
 
 @pytest.mark.parametrize("N,causal,window", [(300, False, 0), (513, True, 0), (700, True, 200)])
 def test_dropout(N, causal, window):
-    """Dropout at d = 256: the forward's keep decisions (tensor-core kernel)
-    and the backward's (CUDA cores, one Philox call per entry) are the
+    """Dropout at d = 256: the keep decisions of the forward and of the
+    backward (both tensor-core kernels, Philox per 4 x 4 patch) are the
     oracle's; bf16 O bound times the keep factor."""
     x = h.seeded(1, 2, N, 256, seed=3700 + N, with_dO=True)
     sc, p, seed = 256 ** -0.5, 0.2, 99 + N

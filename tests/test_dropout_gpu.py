@@ -109,7 +109,7 @@ def test_forward_applies_the_oracle_mask(N, causal, window, d, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N,causal,window", [(128, False, 0), (300, False, 0),
                                              (300, True, 0), (260, True, 100)])
 def test_backward_regenerates_the_oracle_mask(N, causal, window, d, dtype):

@@ -11,11 +11,14 @@
 // The d^2/M wall ("Flash Attention, From First Principles", "The rent
 // arithmetic") in TMEM form: for 128 keys the two accumulators dV and dK
 // alone take 2 x 256 of TMEM's 512 columns, leaving nothing for the score
-// tiles.  So a work item is one head, one block of 128 keys and one HALF of
-// the head dimension, h: it accumulates dV[:, h] and dK[:, h] (128 columns
-// each) and adds dQ[:, h]; the score products S^T = K Q^T and dP^T = V dO^T
-// contract over all 256 columns and are computed by both halves' items (2 of
-// the 5 products twice: 14 of the 10 counted N^2 d units).  Query blocks are
+// tiles.  So a work item (one head, one block of 128 keys) makes two passes
+// over its query blocks, one per HALF of the head dimension, h: pass h
+// accumulates dV[:, h] and dK[:, h] (128 columns each) and adds dQ[:, h];
+// the score products S^T = K Q^T and dP^T = V dO^T contract over all 256
+// columns and are computed in both passes (2 of the 5 products twice: 14 of
+// the 10 counted N^2 d units).  K and V stay loaded across the two passes,
+// and the next item's K and V rows are prefetched into L2 during the second
+// pass.  Query blocks are
 // 64 rows, so that K (64 KiB), a two-stage ring of Q_i and dO_i (4 x 32 KiB)
 // and the dS tile fit in shared memory; V is the A operand of dP^T and lives
 // in TMEM instead (it has no other reader).
@@ -109,12 +112,12 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 
-// Work items: (head, 128-key block kb, half h of d).  Under the causal mask
-// the query blocks of 64 rows visited by key block kb start at 2kb; with a
-// sliding window of w keys they end at the block of the last query whose
-// window still reaches the key block's last key.  Causal cost falls with kb,
-// so items are listed kb-ascending (both halves of a key block side by side)
-// inside head groups and taken in snake waves, as in the d <= 128 backward.
+// Work items: (head, 128-key block kb), each walked twice (once per half of
+// d).  Under the causal mask the query blocks of 64 rows visited by key
+// block kb start at 2kb; with a sliding window of w keys they end at the
+// block of the last query whose window still reaches the key block's last
+// key.  Causal cost falls with kb, so items are listed kb-ascending inside
+// head groups and taken in snake waves, as in the d <= 128 backward.
 struct Sched {
   int BH, N, causal, window, grid;
   int n_kb, n_qb, group, total_items;
@@ -127,12 +130,11 @@ struct Sched {
     grid = grid_size;
     n_kb = (N + 127) / 128;
     n_qb = (N + BQ - 1) / BQ;
-    const int per_head = 2 * n_kb;
-    int g = (causal ? kBwdGroupWaves : 1) * grid / per_head;
+    int g = (causal ? kBwdGroupWaves : 1) * grid / n_kb;
     if (g < 1) g = 1;
     if (g > BH) g = BH;
     group = g;
-    total_items = BH * per_head;
+    total_items = BH * n_kb;
   }
   __host__ __device__ int n_waves() const { return (total_items + grid - 1) / grid; }
   __host__ __device__ int item_of(int cta, int w) const {
@@ -140,8 +142,8 @@ struct Sched {
     const int i = w * grid + pos;
     return i < total_items ? i : -1;
   }
-  __host__ __device__ void decode(int i, int& bh, int& kb, int& h) const {
-    const int per_group = group * 2 * n_kb;
+  __host__ __device__ void decode(int i, int& bh, int& kb) const {
+    const int per_group = group * n_kb;
     const int full_groups = BH / group;
     const int full_items = full_groups * per_group;
     int g, r, gs;
@@ -154,9 +156,7 @@ struct Sched {
       r = i - full_items;
       gs = BH - full_groups * group;
     }
-    const int unit = r / gs;
-    kb = unit >> 1;
-    h = unit & 1;
+    kb = r / gs;
     bh = g * group + r % gs;
   }
   __host__ __device__ int q_begin(int kb) const { return causal ? 2 * kb : 0; }
@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < nw; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
       if (item < 0) continue;
-      int bh0, kb0, h0;
-      sc.decode(item, bh0, kb0, h0);
+      int bh0, kb0;
+      sc.decode(item, bh0, kb0);
       fetch_stats(bh0, sc.q_begin(kb0));
       break;
     }
@@ -338,15 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
       if (item < 0) continue;
-      int bh, kb, h;
-      sc.decode(item, bh, kb, h);
-      int nbh = -1, ni = 0;  // the next item's first block
+      int bh, kb;
+      sc.decode(item, bh, kb);
+      int nbh = -1, nkb = 0, ni = 0;  // the next item and its first block
       for (int w2 = w + 1; w2 < nw; ++w2) {
         const int item2 = sc.item_of(blockIdx.x, w2);
         if (item2 < 0) continue;
-        int kb2, h2;
-        sc.decode(item2, nbh, kb2, h2);
-        ni = sc.q_begin(kb2);
+        sc.decode(item2, nbh, nkb);
+        ni = sc.q_begin(nkb);
         break;
       }
       if (it > 0 && !wait_warp(bar(B_KEMPTY), (it - 1) & 1, abort_flag, lim, SITE_L_KEMPTY))
@@ -358,7 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       k_last = (int)(it & 1);
       const int iend = sc.q_end(kb);
+      for (int h = 0; h < 2 && ok; ++h)
       for (int i = sc.q_begin(kb); i <= iend; ++i) {
+        if (h == 1 && i == sc.q_begin(kb) && nbh >= 0 && lane == 0) {
+          // the next item's K tile into L2 while this item's second pass runs
+          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&mk, c * 64, nkb * 128, nbh);
+        }
         const int s = qcnt % QST;
         const uint32_t ph = (qcnt / QST) & 1;
         float lv[2], dv[2];
@@ -370,6 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i + 1 <= iend)
           fetch_stats(bh, i + 1);
+        else if (h == 0)
+          fetch_stats(bh, sc.q_begin(kb));
         else if (nbh >= 0)
           fetch_stats(nbh, ni);
         // the stage's previous block: its S^T, dP^T, dV and dK products
@@ -413,14 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- tensor core
     if (lane == 0) {
-      uint32_t qcnt = 0, it = 0, g = 0;
+      uint32_t qcnt = 0, it = 0, g = 0, hc = 0;
       bool ok = true;
       const uint32_t sK = sb + OFF_K, sDS = sb + OFF_DS;
       for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
         const int item = sc.item_of(blockIdx.x, w);
         if (item < 0) continue;
-        int bh, kb, h;
-        sc.decode(item, bh, kb, h);
+        int bh, kb;
+        sc.decode(item, bh, kb);
         if (!wait_one(bar(B_KFULL), it & 1, abort_flag, lim, SITE_M_KFULL)) break;
         tc_fence_after();
         const int i0 = sc.q_begin(kb);
@@ -442,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_one(bar(B_VREADY), it & 1, abort_flag, lim, SITE_M_VREADY)) break;
         tc_fence_after();
         const int iend = sc.q_end(kb);
+        for (int h = 0; h < 2 && ok; ++h) {
         for (int i = i0; i <= iend; ++i) {
           const int s = qcnt % QST;
           if (g > 0) {  // dQ^T of the previous block has left TMEM
@@ -464,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const bool first = (i == i0);
-          if (first && it > 0) {  // the previous item's dK, dV have been stored
-            if (!wait_one(bar(B_DKDVFREE), (it - 1) & 1, abort_flag, lim, SITE_M_DKDVFREE)) {
+          if (first && hc > 0) {  // the previous pass's dK, dV have been stored
+            if (!wait_one(bar(B_DKDVFREE), (hc - 1) & 1, abort_flag, lim, SITE_M_DKDVFREE)) {
               ok = false;
               break;
             }
@@ -481,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(bar(B_QEMPTY + s));  // Q_i and dO_i have no later reader
           mma_colsT_x_rows(tmem + TM_DP, sK + 2 * h * kChunkBytes, sDS, IDESC_DQ);
           umma_commit(bar(B_DQFULL));
-          if (i + 1 <= iend && !issue_s(qcnt + 1)) {
+          // the next block's S^T (the first block again after the first pass)
+          if ((i + 1 <= iend || h == 0) && !issue_s(qcnt + 1)) {
             ok = false;
             break;
           }
@@ -489,8 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++g;
         }
         if (!ok) break;
-        umma_commit(bar(B_KEMPTY));
         umma_commit(bar(B_DKDVDONE));
+        ++hc;
+        }
+        if (!ok) break;
+        umma_commit(bar(B_KEMPTY));
         ++it;
       }
       umma_commit(bar(B_MMADONE));
@@ -506,13 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;  // key row (P, dS, dK, dV) / d row (dQ^T)
     const float sl2 = p.scale_log2;
     const float scale = DR ? p.scale * p.drop.keep_scale : p.scale;  // of dP
-    uint32_t qcnt = 0, g = 0, it = 0;
+    uint32_t qcnt = 0, g = 0, hc = 0;
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
       if (item < 0) continue;
-      int bh, kb, h;
-      sc.decode(item, bh, kb, h);
+      int bh, kb;
+      sc.decode(item, bh, kb);
+      // the next item's V row of this thread (this group's 256 bytes) is
+      // brought into L2 during the second pass
+      const __nv_bfloat16* vnext = nullptr;
+      for (int w2 = w + 1; w2 < nw; ++w2) {
+        const int item2 = sc.item_of(blockIdx.x, w2);
+        if (item2 < 0) continue;
+        int nbh, nkb;
+        sc.decode(item2, nbh, nkb);
+        const int nkey = nkb * 128 + r;
+        if (nkey < N) vnext = p.V + ((size_t)nbh * N + (size_t)nkey) * D + 128 * grp;
+        break;
+      }
       const int key = kb * 128 + r;
       const bool kvalid = key < N;
       // V row `key` into TMEM as bf16 pairs: this group's 128 columns of d
@@ -538,6 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(B_VREADY));
       }
       const int iend = sc.q_end(kb);
+      for (int h = 0; h < 2 && ok; ++h) {
+      if (h == 1 && vnext) {
+        prefetch_l2(vnext);
+        prefetch_l2(vnext + 64);
+      }
       for (int i = sc.q_begin(kb); i <= iend; ++i) {
         const int s = qcnt % QST;
         const int q0 = i * BQ + 32 * grp;  // first query of this group's columns
@@ -667,7 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
       if (!ok) break;
-      if (!wait_warp(bar(B_DKDVDONE), it & 1, abort_flag, lim, SITE_E_DKDVDONE)) break;
+      if (!wait_warp(bar(B_DKDVDONE), hc & 1, abort_flag, lim, SITE_E_DKDVDONE)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const bool store = kvalid;
       const size_t rowoff = ((size_t)bh * N + (size_t)(store ? key : 0)) * D + HALF * h;
@@ -694,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(bar(B_DKDVFREE));
-      ++it;
+      ++hc;
+      }
     }
   }
 

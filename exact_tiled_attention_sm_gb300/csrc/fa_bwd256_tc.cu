@@ -39,9 +39,11 @@
 //
 // Roles: warps 0-3 query columns 0-31 of each block, the dV epilogue and
 // V columns 0-127 into TMEM; warps 4-7 query columns 32-63, the dK epilogue
-// and V columns 128-255; warp 8 tensor-core issuer and TMEM owner; warp 9
-// TMA loads (K, Q_i, dO_i) and the per-query statistics (-LSE log2 e,
-// -D scale) of each block.
+// and V columns 128-255; warps 8-11 (the dQ warpgroup) read dQ_h^T out of
+// TMEM and add it to the accumulator, so that the dS warpgroups go from
+// dS(i) straight on to P(i+1) while those adds run; warp 12 tensor-core
+// issuer and TMEM owner; warp 13 TMA loads (K, Q_i, dO_i) and the per-query
+// statistics (-LSE log2 e, -D scale) of each block.
 //
 // TMEM: S^T [0,64), dP^T [64,128), dV_h [128,256), dK_h [256,384),
 // V [384,512) (bf16 pairs).  Warpgroup g writes its P^T into columns
@@ -108,9 +110,10 @@ constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, HALF, 0, 1);
 // dQ_h^T: A = K_h^T and B = dS^T, both MN-major
 constexpr uint32_t IDESC_DQ = idesc_bf16_f32(128, BQ, 1, 1);
 
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kDqWarp0 = 8;   // warps 8-11: the dQ warpgroup
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
 
 // Work items: (head, 128-key block kb), each walked twice (once per half of
 // d).  Under the causal mask the query blocks of 64 rows visited by key
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_PREADY), 256);
     mbar_init(bar(B_DSREADY), 256);
     mbar_init(bar(B_DQFULL), 1);
-    mbar_init(bar(B_DQFREE), 256);
+    mbar_init(bar(B_DQFREE), 128);
     mbar_init(bar(B_VREADY), 256);
     mbar_init(bar(B_DKDVDONE), 1);
     mbar_init(bar(B_DKDVFREE), 256);
@@ -509,8 +512,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_one(bar(B_MMADONE), 0, &no_abort, lim, SITE_DRAIN);
     }
     __syncwarp();
+  } else if (warp >= kDqWarp0 && warp < kDqWarp0 + 4) {
+    // ------------------------------------------------------------ dQ
+    // dQ_h^T: TMEM lanes are d (128h + r), columns the block's 64 queries.
+    // Each block's columns go to registers and are released at once (the
+    // next dP^T is issued into them), then each of the 64 is added into the
+    // accumulator row of its query by a warp-wide red (32 consecutive floats).
+    const int wq = warp - kDqWarp0;  // TMEM lane quarter
+    const uint32_t tmem_row = tmem + ((uint32_t)(wq * 32) << 16);
+    const int r = wq * 32 + lane;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
+      const int item = sc.item_of(blockIdx.x, w);
+      if (item < 0) continue;
+      int bh, kb;
+      sc.decode(item, bh, kb);
+      const int iend = sc.q_end(kb);
+      for (int h = 0; h < 2 && ok; ++h)
+        for (int i = sc.q_begin(kb); i <= iend; ++i) {
+          if (!wait_warp(bar(B_DQFULL), g & 1, abort_flag, lim, SITE_Q_DQFULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t v[2][32];
+          tmem_ld32(tmem_row + TM_DP, v[0]);
+          tmem_ld32(tmem_row + TM_DP + 32, v[1]);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(bar(B_DQFREE));
+          reg_fence32(v[0]);
+          reg_fence32(v[1]);
+          const int q0 = i * BQ;
+          float* dst = p.dQacc + ((size_t)bh * N + (size_t)q0) * D + HALF * h + r;
+          const int nq = min(BQ, N - q0);
+#pragma unroll
+          for (int c = 0; c < BQ; ++c)
+            if (c < nq) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
+          ++g;
+        }
+    }
   } else {
-    // --------------------------------------- dS (both warpgroups), dQ, dK, dV
+    // ------------------------------------------- dS (both warpgroups), dK, dV
     const int grp = warp >> 2;     // query columns [32 grp, 32 grp + 32)
     const int wq = warp & 3;       // TMEM lane quarter
     const uint32_t tmem_row = tmem + ((uint32_t)(wq * 32) << 16);
@@ -670,27 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(B_DSREADY));
-        // ---- dQ_h^T: TMEM lanes are d (128h + r), columns queries; this
-        // group's 32 queries go to registers, the columns are released, and
-        // each is added into the accumulator row by a warp-wide red
-        if (!wait_warp(bar(B_DQFULL), g & 1, abort_flag, lim, SITE_Q_DQFULL)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        {
-          uint32_t v[32];
-          tmem_ld32(tmem_row + TM_DP + 32 * grp, v);
-          tmem_ld_wait();
-          tc_fence_before();
-          mbar_arrive(bar(B_DQFREE));
-          reg_fence32(v);
-          float* dst = p.dQacc + ((size_t)bh * N + (size_t)q0) * D + HALF * h + r;
-          const int nq = min(32, N - q0);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nq) atomicAdd(dst + (size_t)c * D, __uint_as_float(v[c]));
-        }
         ++qcnt;
         ++g;
       }

@@ -69,7 +69,7 @@ def measured_peaks():
 
 # kernel key (as in profiles/traffic.txt) -> the source file that defines it
 KERNEL_SOURCES = {"bwd_kernel": "fa_bwd_tc.cu", "fwd_kernel": "fa_fwd_tc.cu",
-                  "fwd256_kernel": "fa_fwd256_tc.cu"}
+                  "fwd256_kernel": "fa_fwd256_tc.cu", "bwd256_kernel": "fa_bwd256_tc.cu"}
 
 
 def kernel_digest(kernel_key):
@@ -246,7 +246,7 @@ def run_profile(args):
 BALANCE_CASES = (("llama3_8b_fwd", True, "fwd"), ("llama3_8b_fwd", False, "fwd"),
                  ("gpt2_medium_fwd", True, "fwd"), ("gpt2_medium_fwd", False, "fwd"),
                  ("long_ctx_32k", True, "fwd"), ("train_fwd_bwd", True, "fwd"),
-                 ("train_fwd_bwd", True, "bwd"))
+                 ("train_fwd_bwd", True, "bwd"), ("d256_train", True, "bwd"))
 
 
 def run_balance(args):
@@ -281,7 +281,7 @@ def run_balance(args):
         runs = []
         for rep in range(6):
             call()
-            marks = trace.read(L, "fwd256" if (which == "fwd" and w.d == 256) else which)
+            marks = trace.read(L, which + ("256" if w.d == 256 else ""))
             if rep >= 3:
                 runs.append(trace.summarize(marks))
         st = fa.last_device_status()
@@ -552,8 +552,8 @@ def run_ours(args):
             launches += reps
         del q8, k8, v8, of, lf
     # --- head dimension 256: the tensor-core forward (one query block per
-    # item) both ways, and the training step at d = 256, whose backward runs
-    # on the CUDA cores
+    # item) both ways, and the training step at d = 256 (tensor-core backward:
+    # one pass per half of d over 64-query blocks)
     d256_results = {}
     for name, causal_v, passes in (("d256_fwd", False, "fwd"), ("d256_fwd", True, "fwd"),
                                    ("d256_train", True, "fwd+bwd")):

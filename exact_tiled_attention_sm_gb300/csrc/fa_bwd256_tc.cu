@@ -764,8 +764,8 @@ template <bool DR>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
                    const float* Dvec, const void* V, float* dQacc, void* dK, void* dV,
                    int num_sms, uint64_t lim, cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      bwd256_kernel<DR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t attr = smem_limit_once(bwd256_kernel<DR>, SMEM_BYTES, attr_done);
   if (attr != cudaSuccess) return attr;
   Params p;
   p.LSE = LSE;

@@ -733,8 +733,8 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
                    const float* Dvec, void* dK, void* dV, int num_sms,
                    uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D>;
-  static cudaError_t attr = cudaFuncSetAttribute(
-      bwd_kernel<D, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t attr = smem_limit_once(bwd_kernel<D, DR>, C::SMEM_BYTES, attr_done);
   if (attr != cudaSuccess) return attr;
   Params p;
   p.LSE = LSE;

@@ -1,5 +1,6 @@
 // fa_common.cuh -- definitions shared by every kernel translation unit.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -24,6 +25,24 @@ constexpr uint32_t kWaitSleepNs = 20000;
 constexpr int kTile = 128;  // rows of a query block and of a key block
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute belongs to the device's context, so
+// a process that launches on several GPUs needs it on each.  `done` keeps one
+// bit per device ordinal below 64 (higher ordinals set it on every call).
+template <typename Kern>
+cudaError_t smem_limit_once(Kern kernel, int bytes,
+                            std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 }  // namespace fa
 

@@ -466,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool W, bool DR>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O, float* LSE,
                    int num_sms, uint64_t lim, cudaStream_t stream) {
-  static cudaError_t attr = cudaFuncSetAttribute(
-      fwd256_kernel<W, DR>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t attr = smem_limit_once(fwd256_kernel<W, DR>, SMEM_BYTES, attr_done);
   if (attr != cudaSuccess) return attr;
   Params p;
   p.O = reinterpret_cast<__nv_bfloat16*>(O);

@@ -627,14 +627,9 @@ template <int D, bool W, bool DR, bool E8 = false>
 cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
                    float* LSE, int num_sms, uint64_t lim, cudaStream_t stream) {
   using C = Cfg<D, E8>;
-  static bool attr_done = false;  // per process; same value on every device
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(
-        fwd_kernel<D, W, DR, E8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t attr = smem_limit_once(fwd_kernel<D, W, DR, E8>, C::SMEM_BYTES, attr_done);
+  if (attr != cudaSuccess) return attr;
   Params p;
   p.O = reinterpret_cast<__nv_bfloat16*>(O);
   p.LSE = LSE;

@@ -356,11 +356,6 @@ __global__ void selftest_timeout_kernel(uint64_t limit_ns) {
 
 }  // namespace simt
 
-template <typename Kern>
-static cudaError_t smem_attr(Kern k, int bytes) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bytes);
-}
 
 template <int D>
 static cudaError_t fwd_f32_launch(const AttnShape& s, const float* Q,
@@ -368,7 +363,8 @@ static cudaError_t fwd_f32_launch(const AttnShape& s, const float* Q,
                                   float* LSE, cudaStream_t stream) {
   constexpr int bytes =
       (simt::kRows * D + simt::kKeys * (D + 1) + simt::kKeys * D) * 4;
-  static cudaError_t attr = smem_attr(simt::fwd_f32_kernel<D>, bytes);
+  static std::atomic<unsigned long long> attr_done{0};
+  const cudaError_t attr = smem_limit_once(simt::fwd_f32_kernel<D>, bytes, attr_done);
   if (attr != cudaSuccess) return attr;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
   simt::fwd_f32_kernel<D><<<grid, 128, bytes, stream>>>(
@@ -382,9 +378,10 @@ static cudaError_t bwd_f32_launch(const AttnShape& s, const T* Q, const T* K,
                                   const float* Dvec, T* dQ, T* dK, T* dV,
                                   cudaStream_t stream) {
   constexpr int bytes = (2 * simt::kRows * (D + 1) + 2 * simt::kKeys * D) * 4;
-  static cudaError_t a1 = smem_attr(simt::bwd_f32_dkdv_kernel<D, T>, bytes);
-  static cudaError_t a2 = smem_attr(simt::bwd_f32_dq_kernel<D, T>, bytes);
+  static std::atomic<unsigned long long> done1{0}, done2{0};
+  const cudaError_t a1 = smem_limit_once(simt::bwd_f32_dkdv_kernel<D, T>, bytes, done1);
   if (a1 != cudaSuccess) return a1;
+  const cudaError_t a2 = smem_limit_once(simt::bwd_f32_dq_kernel<D, T>, bytes, done2);
   if (a2 != cudaSuccess) return a2;
   dim3 grid((s.N + simt::kRows - 1) / simt::kRows, s.B * s.H);
   simt::bwd_f32_dkdv_kernel<D, T><<<grid, 128, bytes, stream>>>(

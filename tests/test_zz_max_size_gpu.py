@@ -39,3 +39,33 @@ def test_maximum_size_forward_and_backward():
         assert h.rel_l2(h.np64(got[:, hh:hh + 1]), ref) <= h.TOL_GRAD_REL
     del x, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+def test_maximum_size_head_dim_256_forward_and_backward():
+    """The same bound at head dimension 256: 8191 heads of 1024 x 256 (one
+    2^18 short of 2^31 elements), through the d = 256 forward and the
+    tensor-core backward (its items walk each key block twice, once per half
+    of d, and add dQ with reds from registers)."""
+    B, H, N, d = 1, 8191, 1024, 256
+    assert B * H * N * d < 2 ** 31 <= B * (H + 1) * N * d
+    sc = d ** -0.5
+    x = inputs.seeded_inputs_cuda(B, H, N, d, seed=4343, with_dO=True)
+    o, lse = fa.fwd(x["Q"], x["K"], x["V"], sc, True)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    rows = np.array([0, 1, 63, 64, 127, 128, 700, N - 2, N - 1])
+    for hh in (0, H // 2, H - 1):
+        Q, K, V = (inputs.to_f64(x[n][:, hh:hh + 1]) for n in ("Q", "K", "V"))
+        O, L = oracle.fwd_rows(Q, K, V, sc, True, rows)
+        assert h.max_abs(h.np64(o[0, hh])[rows], O) <= h.TOL_O_BF16, hh
+        assert h.max_abs(h.np64(lse[0, hh])[rows], L) <= h.TOL_LSE_BF16, hh
+    dq, dk, dv = fa.bwd(x["Q"], x["K"], x["V"], o, x["dO"], lse, sc, True)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    for hh in (0, H - 1):
+        Q, K, V, dO = (inputs.to_f64(x[n][:, hh:hh + 1]) for n in ("Q", "K", "V", "dO"))
+        dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, True)
+        for got, ref in ((dq, dQ), (dk, dK), (dv, dV)):
+            assert h.rel_l2(h.np64(got[:, hh:hh + 1]), ref) <= h.TOL_GRAD_REL, hh
+    del x, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()

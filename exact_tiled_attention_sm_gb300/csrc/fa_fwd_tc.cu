@@ -5,8 +5,10 @@
 //   warps 0-3  softmax group 0: owns query block 0 of the item (TMEM lanes
 //              0-127, one thread per query row)
 //   warps 4-7  softmax group 1: query block 1
-//   warp  8    tensor-core issuer (one elected thread) and TMEM owner
+//   warp  8    tensor-core issuer of query block 0 (one elected thread) and
+//              TMEM owner
 //   warp  9    TMA producer (one elected thread)
+//   warp 10    tensor-core issuer of query block 1 (one elected thread)
 //
 // Data flow per key/value block j ("LLM Architecture Refresh [3]", section 4:
 // queries outer, key/value blocks inner; "FlashAttention from scratch",
@@ -28,6 +30,17 @@
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d); P_t aliases the first 64 columns of
 // S_t as packed bf16 pairs.
+//
+// At d = 64 (the SA layout) P_t has columns of its own, [384 + 64t, 448 +
+// 64t), so S_t(j+1) no longer waits for P_t V_j: it is issued as soon as the
+// softmax group has read S_t(j) out of TMEM (B_SFREE), and the group goes
+// from block j straight to block j+1, holding P_t(j+1) in registers until
+// P_t V_j has completed (B_PVDONE) and only then writing it (and rescaling
+// O_t, when the reference moved).  Per key block a group then waits for one
+// S product instead of for its P V and S products in turn.  Each query block
+// has its own issuing thread there (warps 8 and 10): with one thread for
+// both, its barrier waits and commits between the bursts left the tensor
+// pipe idle about half the time.
 //
 // With dropout (the DR variant), each softmax thread also draws the keep
 // bytes of its row: per 32-key quarter of a block, two Philox calls per lane
@@ -61,6 +74,12 @@ struct Cfg {
   static constexpr int CHUNK_ELEMS = E8 ? 128 : 64;
   static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = CH * CHUNK_BYTES;
+  static constexpr bool SA = (D == 64) && !E8;   // S ahead of P V (own P columns)
+  static constexpr int NISSUE = SA ? 2 : 1;       // issuing threads
+  static constexpr int THREADS = SA ? 352 : 320;
+  // SA: quarters of P held in registers before the wait for the previous
+  // P V (the later quarters are written as they are computed)
+  static constexpr int P_HELD = 2;
   static constexpr int KST = (CH == 1) ? 4 : 2;  // K ring stages
   static constexpr int VST = (CH == 1) ? 4 : 2;  // V ring stages
   static constexpr int OFF_Q = 0;
@@ -74,13 +93,16 @@ struct Cfg {
   static constexpr int B_SFULL = B_VEMPTY + VST;  // [2]
   static constexpr int B_PREADY = B_SFULL + 2;    // [2]
   static constexpr int B_ODONE = B_PREADY + 2;    // [2]
-  static constexpr int B_MMADONE = B_ODONE + 2;
-  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int B_SFREE = B_ODONE + 2;     // [2] (SA)
+  static constexpr int B_PVDONE = B_SFREE + 2;    // [2] (SA)
+  static constexpr int B_MMADONE = B_PVDONE + 2;  // [2]
+  static constexpr int NBAR = B_MMADONE + 2;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4;
   static constexpr uint32_t TM_S = 0;     // + 128 * t
   static constexpr uint32_t TM_O = 256;   // + D * t
+  static constexpr uint32_t TM_P = SA ? 384 : 0;  // + 64 * t (SA; else P aliases S)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t IDESC_S =
       E8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
@@ -103,9 +125,9 @@ struct Cfg {
   }
 };
 
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;    // issues the products (SA: query block 0's); owns TMEM
 constexpr int kTmaWarp = 9;
+constexpr int kMmaWarp1 = 10;  // (SA) issues query block 1's products
 
 struct Params {
   __nv_bfloat16* O;
@@ -121,14 +143,14 @@ struct Params {
 enum : uint32_t {
   SITE_P_QEMPTY = 1, SITE_P_KEMPTY, SITE_P_VEMPTY, SITE_M_QFULL, SITE_M_KFULL,
   SITE_M_VFULL, SITE_M_PREADY, SITE_S_SFULL, SITE_S_ODONE, SITE_DRAIN,
-  SITE_ALIGN
+  SITE_ALIGN, SITE_M_SFREE, SITE_S_PVDONE
 };
 
 // W: the causal sliding-window variant, DR: dropout, E8: E4M3 inputs (each
 // compiled separately, so that the plain kernels carry none of their
 // bookkeeping).
 template <int D, bool W, bool DR, bool E8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, const Params p) {
@@ -146,22 +168,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t lim = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
+    // the empty barriers take one commit from each issuing thread
     mbar_init(bar(C::B_QFULL), 1);
-    mbar_init(bar(C::B_QEMPTY), 1);
+    mbar_init(bar(C::B_QEMPTY), C::NISSUE);
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), C::NISSUE);
     }
     for (int s = 0; s < C::VST; ++s) {
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), C::NISSUE);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
       mbar_init(bar(C::B_PREADY + t), 128);
       mbar_init(bar(C::B_ODONE + t), 1);
+      mbar_init(bar(C::B_SFREE + t), 128);
+      mbar_init(bar(C::B_PVDONE + t), 1);
     }
     mbar_init(bar(C::B_MMADONE), 1);
+    mbar_init(bar(C::B_MMADONE + 1), 1);
     // the swizzled tiles need 1024-byte alignment: refuse to run otherwise
     *abort_flag = (sb & 1023u) ? 1 : 0;
     if (sb & 1023u) record_timeout(abort_flag, SITE_ALIGN);
@@ -267,8 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    SITE_DRAIN);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (!C::SA && warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor core
+    // One issuing thread for both query blocks, in the order P_0 V_j,
+    // S_0(j+1), P_1 V_j, S_1(j+1): each block's two products run as one burst
+    // while the other block's softmax works.
     if (lane == 0) {
       uint32_t kcnt = 0, vcnt = 0, it = 0;
       uint32_t pcnt0 = 0, pcnt1 = 0;
@@ -372,6 +401,141 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_one(bar(C::B_MMADONE), 0, &no_abort, lim, SITE_DRAIN);
     }
     __syncwarp();
+  } else if (C::SA && (warp == kMmaWarp || warp == kMmaWarp1)) {
+    // ------------------------------------------------------------ tensor core
+    // (SA) One issuing thread per query block t, so that one thread's barrier
+    // waits and commits overlap the other's products in the tensor pipe
+    // (with S_t(j+1) issued ahead of P_t V_j, neither block waits for the
+    // other's burst).  Both walk every key block of the item: the K/V ring
+    // stages and the Q tiles are released by one commit from each (after
+    // each has seen the stage filled), whether or not its query block reads
+    // that key block.
+    if (lane == 0) {
+      const int t = warp == kMmaWarp ? 0 : 1;
+      uint32_t kcnt = 0, vcnt = 0, it = 0;
+      uint32_t pc = 0;  // P-ready phases consumed
+      uint32_t si = 0;  // S_t products issued so far
+      // S_t is overwritten only after the softmax group has read the
+      // previous S_t out of TMEM
+      auto s_free = [&]() -> bool {
+        if (si > 0) {
+          if (!wait_one(bar(C::B_SFREE + t), (si - 1) & 1, abort_flag, lim,
+                        SITE_M_SFREE))
+            return false;
+          tc_fence_after();
+        }
+        ++si;
+        return true;
+      };
+      const uint32_t tS = tmem + C::TM_S + 128 * t;
+      const uint32_t tO = tmem + C::TM_O + D * t;
+      const uint32_t tP = tmem + C::TM_P + 64 * t;
+      const int nw = sc.n_waves();
+      for (int w = 0; w < nw && !*abort_flag; ++w) {
+        const int item = sc.item_of(blockIdx.x, w);
+        if (item < 0) continue;
+        int bh, pair;
+        sc.decode(item, bh, pair);
+        const int q0 = 2 * pair;
+        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        // key-block range of each query block (tile 1's may start one block
+        // later and ends one later under the causal mask; empty if absent)
+        const int lo0 = W ? sc.kv_lo(q0) : 0, hi0 = sc.kv_hi(q0);
+        const int lo1 = (W && valid1) ? sc.kv_lo(q0 + 1) : 0;
+        const int hi1 = valid1 ? sc.kv_hi(q0 + 1) : -1;
+        const int jlo = lo0, jhi = hi1 > hi0 ? hi1 : hi0;
+        const int lo = t ? lo1 : lo0, hi = t ? hi1 : hi0;
+        auto mine = [&](int j) { return j >= lo && j <= hi; };
+        bool ok = wait_one(bar(C::B_QFULL), it & 1, abort_flag, lim, SITE_M_QFULL);
+        if (!ok) break;
+        tc_fence_after();
+        {  // S_t for the first key block
+          const int s = kcnt % C::KST;
+          if (!wait_one(bar(C::B_KFULL + s), (kcnt / C::KST) & 1, abort_flag,
+                        lim, SITE_M_KFULL))
+            break;
+          tc_fence_after();
+          if (mine(jlo)) {
+            if (!s_free()) break;
+            C::mma_s(tS, sQ(t), sb + C::OFF_K + s * C::TILE_BYTES);
+            umma_commit(bar(C::B_SFULL + t));
+          }
+          umma_commit(bar(C::B_KEMPTY + s));
+          ++kcnt;
+          // the Q tiles are read by S products only: with a single key block
+          // they are free for the next item as soon as these complete
+          if (jlo == jhi) umma_commit(bar(C::B_QEMPTY));
+        }
+        for (int j = jlo; j <= jhi && ok; ++j) {
+          const int vs = vcnt % C::VST;
+          if (!wait_one(bar(C::B_VFULL + vs), (vcnt / C::VST) & 1, abort_flag,
+                        lim, SITE_M_VFULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sv = sb + C::OFF_V + vs * C::TILE_BYTES;
+          const bool next = j + 1 <= jhi;  // the item has key block j + 1
+          const int ks = kcnt % C::KST;
+          const uint32_t sk = sb + C::OFF_K + ks * C::TILE_BYTES;
+          bool k_ready = false;
+          auto k_wait = [&]() -> bool {
+            if (k_ready) return true;
+            if (!wait_one(bar(C::B_KFULL + ks), (kcnt / C::KST) & 1, abort_flag,
+                          lim, SITE_M_KFULL))
+              return false;
+            tc_fence_after();
+            k_ready = true;
+            return true;
+          };
+          // O_t += P_t V_j once the softmax group has written P_t
+          auto do_pv = [&]() -> bool {
+            if (!mine(j)) return true;
+            if (!wait_one(bar(C::B_PREADY + t), pc & 1, abort_flag, lim,
+                          SITE_M_PREADY))
+              return false;
+            ++pc;
+            tc_fence_after();
+            C::mma_pv(tO, tP, sv, j > lo);
+            umma_commit(bar(C::B_PVDONE + t));
+            if (j == hi) umma_commit(bar(C::B_ODONE + t));
+            return true;
+          };
+          // S_t = Q_t K_{j+1}^T
+          auto do_s = [&]() -> bool {
+            if (!mine(j + 1)) return true;
+            if (!k_wait()) return false;
+            if (!s_free()) return false;
+            C::mma_s(tS, sQ(t), sk);
+            umma_commit(bar(C::B_SFULL + t));
+            return true;
+          };
+          // S_t(j+1) first: P_t V_j reads P_t's own columns
+          ok = do_s() && do_pv();
+          if (!ok) break;
+          umma_commit(bar(C::B_VEMPTY + vs));
+          ++vcnt;
+          if (next) {  // released only once this thread has seen it filled
+            if (!k_wait()) {
+              ok = false;
+              break;
+            }
+            umma_commit(bar(C::B_KEMPTY + ks));
+            ++kcnt;
+          }
+          // the item's last S products have been issued: the next item's Q
+          // tiles may load while its last P V products and epilogue run
+          if (j + 1 == jhi) umma_commit(bar(C::B_QEMPTY));
+        }
+        if (!ok) break;
+        ++it;
+      }
+      // every MMA issued by this thread completes before TMEM is released
+      umma_commit(bar(C::B_MMADONE + t));
+      volatile int no_abort = 0;
+      wait_one(bar(C::B_MMADONE + t), 0, &no_abort, lim, SITE_DRAIN);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;          // query block of the item
@@ -379,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::TM_S + 128 * t;
     const uint32_t tO = tmem + lane_off + C::TM_O + D * t;
+    const uint32_t tP = C::SA ? tmem + lane_off + C::TM_P + 64 * t : tS;
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, ocnt = 0;
     const int nw = sc.n_waves();
@@ -413,6 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence32(r1);
         reg_fence32(r2);
         reg_fence32(r3);
+        if constexpr (C::SA) {  // S_t may take the next block's product now
+          tc_fence_before();
+          mbar_arrive(bar(C::B_SFREE + t));
+        }
         float x[128];  // raw scores q.k of this row
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -483,12 +652,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // did).  O's first 64 columns are requested (always, which keeps the
         // register allocation free of branches) before the last quarter of
         // the exponentials, so that their TMEM latency hides behind it.
+        // (SA: the previous P V may still run; O and P_t are touched only
+        // after it has completed, below.)
         const bool resc = j > jlo && __any_sync(0xffffffffu, alpha != 1.f);
         uint32_t oa[2][32];
+        uint32_t pks[4][16];  // P of this row, 32 keys per quarter
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        bool pv_ok = true;
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          if (h == 3) {
+          if constexpr (C::SA) {
+            if (h == C::P_HELD) {
+              // P_t and O_t are free once the group's previous P V has
+              // completed; the quarters held so far are written then
+              const uint32_t b = scnt - 1;  // this block's index in the group
+              if (b > 0) {
+                pv_ok = wait_warp(bar(C::B_PVDONE + t), (b - 1) & 1, abort_flag,
+                                  lim, SITE_S_PVDONE);
+                if (!pv_ok) break;
+                tc_fence_after();
+              }
+#pragma unroll
+              for (int h2 = 0; h2 < C::P_HELD; ++h2) tmem_st16(tP + 16 * h2, pks[h2]);
+            }
+          }
+          if (h == 3 && !C::SA) {
             tmem_ld32(tO + 0, oa[0]);
             tmem_ld32(tO + 32, oa[1]);
           }
@@ -508,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < 4; ++c) kw[4 * g + c] = keep_flags(a[c], p.drop);
             }
           }
-          uint32_t pk[16];
+          uint32_t(&pk)[16] = pks[h];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int e = 32 * h + 2 * i;
@@ -529,17 +717,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int w = 0; w < 8; ++w) p8[w] = __byte_perm(pk[2 * w], pk[2 * w + 1], 0x5410);
             tmem_st8(tS + 8 * h, p8);
-          } else {
+          } else if constexpr (!C::SA) {
             tmem_st16(tS + 16 * h, pk);
+          } else {
+            if (h >= C::P_HELD) tmem_st16(tP + 16 * h, pk);
           }
+        }
+        if (!pv_ok) {
+          ok = false;
+          break;
         }
         float rs_lo, rs_hi;
         f2_unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), rs_lo, rs_hi);
         l = l * alpha + (rs_lo + rs_hi);
-        // the loaded registers stay untouched until the load has landed
-        tmem_ld_wait();
-        reg_fence32(oa[0]);
-        reg_fence32(oa[1]);
+        if constexpr (C::SA) {
+          if (resc) {
+            tmem_ld32(tO + 0, oa[0]);
+            tmem_ld32(tO + 32, oa[1]);
+            tmem_ld_wait();
+            reg_fence32(oa[0]);
+            reg_fence32(oa[1]);
+          }
+        } else {
+          // the loaded registers stay untouched until the load has landed
+          tmem_ld_wait();
+          reg_fence32(oa[0]);
+          reg_fence32(oa[1]);
+        }
         if (resc) {
           const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
@@ -642,7 +846,7 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   probe.init(BH, s.N, s.causal, num_sms, s.window);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  fwd_kernel<D, W, DR, E8><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
+  fwd_kernel<D, W, DR, E8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }

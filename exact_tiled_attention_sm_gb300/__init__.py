@@ -23,7 +23,7 @@ EXPORTS = ("fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_fwd_window",
            "fa_last_device_status",
            "fa_status_string", "fa_selftest_wait_timeout",
            "fa_fwd_schedule_census", "fa_fwd_schedule_census_window",
-           "fa_version")
+           "fa_fwd_schedule_cover", "fa_version")
 
 _lib = None
 
@@ -96,6 +96,9 @@ def lib():
         L.fa_selftest_wait_timeout.restype = i
         L.fa_fwd_schedule_census.argtypes = [i, i, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_fwd_schedule_census.restype = i
+        L.fa_fwd_schedule_cover.argtypes = [i, i, i, i, i, ctypes.POINTER(i),
+                                            ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.fa_fwd_schedule_cover.restype = i
         L.fa_version.argtypes = []
         L.fa_version.restype = i
         _lib = L
@@ -195,6 +198,19 @@ def fa_fwd_schedule_census_window(N, causal, window):
     if st != FA_OK:
         raise FAError(st, "fa_fwd_schedule_census_window")
     return tuple(out)
+
+
+def fa_fwd_schedule_cover(BH, N, causal, window, num_sms):
+    """(counts per (head, query block) as a BH x ceil(N/128) list of lists,
+    grid, items) of the forward launch's work list."""
+    nq = (N + 127) // 128
+    counts = (ctypes.c_int * (BH * nq))()
+    grid, items = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().fa_fwd_schedule_cover(BH, N, int(causal), int(window), num_sms, counts,
+                                     ctypes.byref(grid), ctypes.byref(items))
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd_schedule_cover")
+    return [list(counts[b * nq:(b + 1) * nq]) for b in range(BH)], grid.value, items.value
 
 
 def fa_version():

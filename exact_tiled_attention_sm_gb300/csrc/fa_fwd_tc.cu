@@ -220,10 +220,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
       for (int w = 0; w < nw && !*abort_flag; ++w) {
         const int item = sc.item_of(blockIdx.x, w);
         if (item < 0) continue;
-        int bh, pair;
-        sc.decode(item, bh, pair);
-        const int q0 = 2 * pair;
-        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        int bh;
+        int q0;
+        bool valid1;  // the item holds query block q0 + 1 as well
+        sc.decode_blocks(item, bh, q0, valid1);
         // key blocks of either query block: kv_lo(q0) .. kv_hi(last)
         const int jlo = W ? sc.kv_lo(q0) : 0;
         const int jhi = sc.kv_hi(valid1 ? q0 + 1 : q0);
@@ -305,10 +305,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
       for (int w = 0; w < nw && !*abort_flag; ++w) {
         const int item = sc.item_of(blockIdx.x, w);
         if (item < 0) continue;
-        int bh, pair;
-        sc.decode(item, bh, pair);
-        const int q0 = 2 * pair;
-        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        int bh;
+        int q0;
+        bool valid1;  // the item holds query block q0 + 1 as well
+        sc.decode_blocks(item, bh, q0, valid1);
         // key-block range of each query block (tile 1's may start one block
         // later and ends one later under the causal mask; empty if absent)
         const int lo0 = W ? sc.kv_lo(q0) : 0, hi0 = sc.kv_hi(q0);
@@ -434,10 +434,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
       for (int w = 0; w < nw && !*abort_flag; ++w) {
         const int item = sc.item_of(blockIdx.x, w);
         if (item < 0) continue;
-        int bh, pair;
-        sc.decode(item, bh, pair);
-        const int q0 = 2 * pair;
-        const bool valid1 = (q0 + 1) < sc.n_q_tiles;
+        int bh;
+        int q0;
+        bool valid1;  // the item holds query block q0 + 1 as well
+        sc.decode_blocks(item, bh, q0, valid1);
         // key-block range of each query block (tile 1's may start one block
         // later and ends one later under the causal mask; empty if absent)
         const int lo0 = W ? sc.kv_lo(q0) : 0, hi0 = sc.kv_hi(q0);
@@ -550,10 +550,12 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
     for (int w = 0; w < nw && !*abort_flag; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
       if (item < 0) continue;
-      int bh, pair;
-      sc.decode(item, bh, pair);
-      const int q = 2 * pair + t;
-      if (q >= sc.n_q_tiles) continue;
+      int bh;
+      int q0;
+      bool two;
+      sc.decode_blocks(item, bh, q0, two);
+      if (t == 1 && !two) continue;
+      const int q = q0 + t;
       const int jlo = W ? sc.kv_lo(q) : 0, jhi = sc.kv_hi(q);
       const int row = q * 128 + wq * 32 + lane;
       float m = -INFINITY;     // running row maximum of the raw scores
@@ -842,10 +844,8 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   p.v_descale = s.v_descale;
   p.drop = s.drop;
   const int BH = s.B * s.H;
-  FwdSched probe;
-  probe.init(BH, s.N, s.causal, num_sms, s.window);
-  const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
-  p.sched.init(BH, s.N, s.causal, grid, s.window);
+  p.sched = FwdSched::planned(BH, s.N, s.causal, num_sms, s.window);
+  const int grid = p.sched.grid;
   fwd_kernel<D, W, DR, E8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, p);
   return cudaGetLastError();

@@ -16,7 +16,11 @@
 // Balance.  Causal items cost in proportion to (pair + 1), so within a group
 // of heads items are listed heaviest first, and a persistent grid takes the
 // list in waves of `grid` items with the CTA order reversed on every other
-// wave ("snake"), pairing heavy with light items.  Locality.  The list is
+// wave ("snake"), pairing heavy with light items.  Without a mask every item
+// costs the same and only the last, partial wave is uneven: when its pairs
+// fill at most half a wave, each is split into its two query blocks, which
+// the CTAs then take one each (a single-block item runs one softmax group
+// and finishes sooner).  Locality.  The list is
 // grouped by heads, `group` heads (about kGroupWaves waves of items) at a
 // time, so the K/V blocks that the running CTAs stream are shared through L2
 // instead of re-read from HBM.
@@ -41,6 +45,7 @@ constexpr int kBwdGroupWaves = 4;
 struct FwdSched {
   int BH, N, causal, window, grid;
   int n_q_tiles, n_pairs, n_kv_total, group, total_items;
+  int split_from;  // items from here on are single query blocks of split pairs
 
   // window > 0: causal sliding window of `window` keys (implies causal).
   // n_pairs counts the items of one head (pairs, or blocks when
@@ -60,6 +65,24 @@ struct FwdSched {
     if (g > BH) g = BH;
     group = g;
     total_items = BH * n_pairs;
+    split_from = total_items;
+    const int tail = total_items % grid;
+    if (blocks_per_item == 2 && !causal && (n_q_tiles & 1) == 0 && tail > 0 &&
+        2 * tail <= grid) {
+      split_from = total_items - tail;
+      total_items += tail;
+    }
+  }
+
+  // The forward launch's schedule: a grid of num_sms CTAs, or one CTA per
+  // item when the items do not fill it (two-block items).
+  static FwdSched planned(int bh, int n, int is_causal, int num_sms, int win = 0) {
+    FwdSched probe;
+    probe.init(bh, n, is_causal, num_sms, win);
+    FwdSched sc;
+    sc.init(bh, n, is_causal,
+            probe.total_items < num_sms ? probe.total_items : num_sms, win);
+    return sc;
   }
 
   // Number of waves a CTA walks through.
@@ -91,6 +114,18 @@ struct FwdSched {
     }
     pair = n_pairs - 1 - r / gs;  // heaviest pairs first within a group
     bh = g * group + r % gs;
+  }
+
+  // Item index -> (flat head bh, first query block q0, whether the item also
+  // holds block q0 + 1), for items of up to two blocks.
+  __host__ __device__ __forceinline__ void decode_blocks(int i, int& bh, int& q0,
+                                                        bool& two) const {
+    int pair;
+    const bool single = i >= split_from;
+    const int u = i - split_from;
+    decode(single ? split_from + (u >> 1) : i, bh, pair);
+    q0 = 2 * pair + (single ? (u & 1) : 0);
+    two = !single && (2 * pair + 1 < n_q_tiles);
   }
 
   // First and last key block visited by query block q (q < n_q_tiles).

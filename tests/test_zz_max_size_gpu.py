@@ -69,3 +69,33 @@ def test_maximum_size_head_dim_256_forward_and_backward():
             assert h.rel_l2(h.np64(got[:, hh:hh + 1]), ref) <= h.TOL_GRAD_REL, hh
     del x, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
+
+
+def test_maximum_size_head_dim_64_forward_and_backward():
+    """The same bound at head dimension 64: 8191 heads of 4096 x 64, through
+    the d = 64 forward (S issued ahead of P V, one issuing thread per query
+    block) and the tensor-core backward."""
+    B, H, N, d = 1, 8191, 4096, 64
+    assert B * H * N * d < 2 ** 31 <= B * (H + 1) * N * d
+    sc = d ** -0.5
+    x = inputs.seeded_inputs_cuda(B, H, N, d, seed=4444, with_dO=True)
+    for causal in (False, True):
+        o, lse = fa.fwd(x["Q"], x["K"], x["V"], sc, causal)
+        torch.cuda.synchronize()
+        assert fa.last_device_status() == fa.FA_OK
+        rows = np.array([0, 1, 127, 128, 255, 256, 2047, 4000, N - 2, N - 1])
+        for hh in (0, H // 2, H - 1):
+            Q, K, V = (inputs.to_f64(x[n][:, hh:hh + 1]) for n in ("Q", "K", "V"))
+            O, L = oracle.fwd_rows(Q, K, V, sc, causal, rows)
+            assert h.max_abs(h.np64(o[0, hh])[rows], O) <= h.TOL_O_BF16, (causal, hh)
+            assert h.max_abs(h.np64(lse[0, hh])[rows], L) <= h.TOL_LSE_BF16, (causal, hh)
+    dq, dk, dv = fa.bwd(x["Q"], x["K"], x["V"], o, x["dO"], lse, sc, True)
+    torch.cuda.synchronize()
+    assert fa.last_device_status() == fa.FA_OK
+    hh = H - 1
+    Q, K, V, dO = (inputs.to_f64(x[n][:, hh:hh + 1]) for n in ("Q", "K", "V", "dO"))
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, True)
+    for got, ref in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert h.rel_l2(h.np64(got[:, hh:hh + 1]), ref) <= h.TOL_GRAD_REL
+    del x, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()

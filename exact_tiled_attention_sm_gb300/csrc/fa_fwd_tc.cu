@@ -462,9 +462,10 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
           }
           umma_commit(bar(C::B_KEMPTY + s));
           ++kcnt;
-          // the Q tiles are read by S products only: with a single key block
-          // they are free for the next item as soon as these complete
-          if (jlo == jhi) umma_commit(bar(C::B_QEMPTY));
+          // the Q tiles are read by S products only: this thread releases
+          // them after its own last S of the item (here when that was the
+          // first, or when its query block is absent from the item)
+          if (hi == jlo || hi < lo) umma_commit(bar(C::B_QEMPTY));
         }
         for (int j = jlo; j <= jhi && ok; ++j) {
           const int vs = vcnt % C::VST;
@@ -511,7 +512,9 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
             return true;
           };
           // S_t(j+1) first: P_t V_j reads P_t's own columns
-          ok = do_s() && do_pv();
+          ok = do_s();
+          if (ok && j + 1 == hi) umma_commit(bar(C::B_QEMPTY));  // its last S
+          ok = ok && do_pv();
           if (!ok) break;
           umma_commit(bar(C::B_VEMPTY + vs));
           ++vcnt;
@@ -523,9 +526,6 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
             umma_commit(bar(C::B_KEMPTY + ks));
             ++kcnt;
           }
-          // the item's last S products have been issued: the next item's Q
-          // tiles may load while its last P V products and epilogue run
-          if (j + 1 == jhi) umma_commit(bar(C::B_QEMPTY));
         }
         if (!ok) break;
         ++it;

@@ -96,7 +96,7 @@ def lib():
         L.fa_selftest_wait_timeout.restype = i
         L.fa_fwd_schedule_census.argtypes = [i, i, ctypes.POINTER(ctypes.c_longlong)]
         L.fa_fwd_schedule_census.restype = i
-        L.fa_fwd_schedule_cover.argtypes = [i, i, i, i, i, ctypes.POINTER(i),
+        L.fa_fwd_schedule_cover.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i),
                                             ctypes.POINTER(i), ctypes.POINTER(i)]
         L.fa_fwd_schedule_cover.restype = i
         L.fa_version.argtypes = []
@@ -200,14 +200,14 @@ def fa_fwd_schedule_census_window(N, causal, window):
     return tuple(out)
 
 
-def fa_fwd_schedule_cover(BH, N, causal, window, num_sms):
+def fa_fwd_schedule_cover(BH, N, causal, window, num_sms, d=128):
     """(counts per (head, query block) as a BH x ceil(N/128) list of lists,
     grid, items) of the forward launch's work list."""
     nq = (N + 127) // 128
     counts = (ctypes.c_int * (BH * nq))()
     grid, items = ctypes.c_int(0), ctypes.c_int(0)
-    st = lib().fa_fwd_schedule_cover(BH, N, int(causal), int(window), num_sms, counts,
-                                     ctypes.byref(grid), ctypes.byref(items))
+    st = lib().fa_fwd_schedule_cover(BH, N, int(causal), int(window), int(d), num_sms,
+                                     counts, ctypes.byref(grid), ctypes.byref(items))
     if st != FA_OK:
         raise FAError(st, "fa_fwd_schedule_cover")
     return [list(counts[b * nq:(b + 1) * nq]) for b in range(BH)], grid.value, items.value

@@ -441,28 +441,35 @@ FA_API fa_status fa_fwd_schedule_census_window(int N, int causal, int window,
   return FA_OK;
 }
 
-FA_API fa_status fa_fwd_schedule_cover(int BH, int N, int causal, int window,
+FA_API fa_status fa_fwd_schedule_cover(int BH, int N, int causal, int window, int d,
                                        int num_sms, int* counts, int* grid,
                                        int* items) {
   if (BH < 1 || N < 1 || window < 0 || num_sms < 1 || !counts) return FA_ERR_INVALID_ARG;
-  const fa::FwdSched sc =
-      fa::FwdSched::planned(BH, N, causal ? 1 : 0, num_sms, window < N ? window : 0);
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const int win = window < N ? window : 0;
+  // d = 64: single-block items for two workers per CTA; d = 128: pairs
+  const bool groups = d == 64;
+  const fa::FwdSched sc = groups ? fa::FwdSched::planned_groups(BH, N, causal ? 1 : 0, num_sms, win)
+                                 : fa::FwdSched::planned(BH, N, causal ? 1 : 0, num_sms, win);
   const size_t n = (size_t)BH * sc.n_q_tiles;
   for (size_t i = 0; i < n; ++i) counts[i] = 0;
   const int nw = sc.n_waves();
-  for (int cta = 0; cta < sc.grid; ++cta)
+  for (int v = 0; v < sc.grid; ++v)
     for (int w = 0; w < nw; ++w) {
-      const int item = sc.item_of(cta, w);
+      const int item = sc.item_of(v, w);
       if (item < 0) continue;
       int bh, q0;
-      bool two;
-      sc.decode_blocks(item, bh, q0, two);
+      bool two = false;
+      if (groups)
+        sc.decode(item, bh, q0);
+      else
+        sc.decode_blocks(item, bh, q0, two);
       if (bh < 0 || bh >= BH || q0 < 0 || q0 + (two ? 1 : 0) >= sc.n_q_tiles)
         return FA_ERR_INVALID_ARG;  // an item outside the tensor
       ++counts[(size_t)bh * sc.n_q_tiles + q0];
       if (two) ++counts[(size_t)bh * sc.n_q_tiles + q0 + 1];
     }
-  if (grid) *grid = sc.grid;
+  if (grid) *grid = groups ? sc.grid / 2 : sc.grid;
   if (items) *items = sc.total_items;
   return FA_OK;
 }

@@ -5,10 +5,11 @@
 //   warps 0-3  softmax group 0: owns query block 0 of the item (TMEM lanes
 //              0-127, one thread per query row)
 //   warps 4-7  softmax group 1: query block 1
-//   warp  8    tensor-core issuer of query block 0 (one elected thread) and
-//              TMEM owner
+//   warp  8    tensor-core issuer (one elected thread) and TMEM owner
 //   warp  9    TMA producer (one elected thread)
-//   warp 10    tensor-core issuer of query block 1 (one elected thread)
+// At d = 64 (SA, below) the two groups are independent pipelines, each with
+// its own items (single query blocks), Q tile and K/V ring: warps 8 and 10
+// issue the products of groups 0 and 1, warps 9 and 11 load their tiles.
 //
 // Data flow per key/value block j ("LLM Architecture Refresh [3]", section 4:
 // queries outer, key/value blocks inner; "FlashAttention from scratch",
@@ -37,10 +38,13 @@
 // from block j straight to block j+1, holding P_t(j+1) in registers until
 // P_t V_j has completed (B_PVDONE) and only then writing it (and rescaling
 // O_t, when the reference moved).  Per key block a group then waits for one
-// S product instead of for its P V and S products in turn.  Each query block
-// has its own issuing thread there (warps 8 and 10): with one thread for
-// both, its barrier waits and commits between the bursts left the tensor
-// pipe idle about half the time.
+// S product instead of for its P V and S products in turn.  Each group has
+// its own issuing thread (with one thread for both, its barrier waits and
+// commits between the bursts left the tensor pipe idle about half the time)
+// and its own loads: group g is worker g * CTAs + cta of a schedule of
+// single query blocks (FwdSched::planned_groups), with a 3-stage K/V ring
+// of its own, so one group's item boundary and epilogue overlap the other
+// group's blocks, and causal items are half as coarse.
 //
 // With dropout (the DR variant), each softmax thread also draws the keep
 // bytes of its row: per 32-key quarter of a block, two Philox calls per lane
@@ -74,23 +78,27 @@ struct Cfg {
   static constexpr int CHUNK_ELEMS = E8 ? 128 : 64;
   static constexpr int CHUNK_BYTES = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = CH * CHUNK_BYTES;
-  static constexpr bool SA = (D == 64) && !E8;   // S ahead of P V (own P columns)
-  static constexpr int NISSUE = SA ? 2 : 1;       // issuing threads
-  static constexpr int THREADS = SA ? 352 : 320;
+  // SA (d = 64): S ahead of P V (P in its own TMEM columns), and the two
+  // query-block groups as independent pipelines (own producer, issuer, Q
+  // tile, K/V ring and stream of single-block items).
+  static constexpr bool SA = (D == 64) && !E8;
+  static constexpr int THREADS = SA ? 384 : 320;
   // SA: quarters of P held in registers before the wait for the previous
   // P V (the later quarters are written as they are computed)
   static constexpr int P_HELD = 2;
-  static constexpr int KST = (CH == 1) ? 4 : 2;  // K ring stages
-  static constexpr int VST = (CH == 1) ? 4 : 2;  // V ring stages
-  static constexpr int OFF_Q = 0;
+  static constexpr int NRING = SA ? 2 : 1;                 // K/V rings
+  static constexpr int KST = SA ? 3 : ((CH == 1) ? 4 : 2);  // K stages per ring
+  static constexpr int VST = KST;                          // V stages per ring
+  static constexpr int OFF_Q = 0;  // Q tiles of query blocks (groups) 0, 1
   static constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
-  // barrier slots
-  static constexpr int B_QFULL = 0, B_QEMPTY = 1;
-  static constexpr int B_KFULL = 2, B_KEMPTY = B_KFULL + KST;
-  static constexpr int B_VFULL = B_KEMPTY + KST, B_VEMPTY = B_VFULL + VST;
-  static constexpr int B_SFULL = B_VEMPTY + VST;  // [2]
+  static constexpr int OFF_V = OFF_K + NRING * KST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NRING * VST * TILE_BYTES;
+  // barrier slots (the Q and ring barriers of group g at + g under SA)
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2;  // [2]
+  static constexpr int B_KFULL = 4, B_KEMPTY = B_KFULL + NRING * KST;
+  static constexpr int B_VFULL = B_KEMPTY + NRING * KST;
+  static constexpr int B_VEMPTY = B_VFULL + NRING * VST;
+  static constexpr int B_SFULL = B_VEMPTY + NRING * VST;  // [2]
   static constexpr int B_PREADY = B_SFULL + 2;    // [2]
   static constexpr int B_ODONE = B_PREADY + 2;    // [2]
   static constexpr int B_SFREE = B_ODONE + 2;     // [2] (SA)
@@ -125,9 +133,10 @@ struct Cfg {
   }
 };
 
-constexpr int kMmaWarp = 8;    // issues the products (SA: query block 0's); owns TMEM
-constexpr int kTmaWarp = 9;
-constexpr int kMmaWarp1 = 10;  // (SA) issues query block 1's products
+constexpr int kMmaWarp = 8;    // issues the products (SA: group 0's); owns TMEM
+constexpr int kTmaWarp = 9;    // loads (SA: group 0's)
+constexpr int kMmaWarp1 = 10;  // (SA) issues group 1's products
+constexpr int kTmaWarp1 = 11;  // (SA) loads group 1's tiles
 
 struct Params {
   __nv_bfloat16* O;
@@ -168,16 +177,17 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
   const uint64_t lim = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
-    // the empty barriers take one commit from each issuing thread
-    mbar_init(bar(C::B_QFULL), 1);
-    mbar_init(bar(C::B_QEMPTY), C::NISSUE);
-    for (int s = 0; s < C::KST; ++s) {
-      mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), C::NISSUE);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar(C::B_QFULL + g), 1);
+      mbar_init(bar(C::B_QEMPTY + g), 1);
     }
-    for (int s = 0; s < C::VST; ++s) {
+    for (int s = 0; s < C::NRING * C::KST; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NRING * C::VST; ++s) {
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), C::NISSUE);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SFULL + t), 1);
@@ -205,7 +215,87 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
 
   auto sQ = [&](int t) { return sb + C::OFF_Q + (uint32_t)t * C::TILE_BYTES; };
 
-  if (warp == kTmaWarp) {
+  if (C::SA && (warp == kTmaWarp || warp == kTmaWarp1)) {
+    // ------------------------------------------------------------ producer
+    // (SA) Group g's loads: its Q tile, then its K/V blocks through its own
+    // ring, for the single-block items of worker g*grid + cta.
+    if (lane == 0) {
+      const int g = warp == kTmaWarp ? 0 : 1;
+      const int v = g * (int)gridDim.x + (int)blockIdx.x;
+      if (g == 0) {
+        prefetch_tensormap(&mq);
+        prefetch_tensormap(&mk);
+        prefetch_tensormap(&mv);
+      }
+      uint32_t kcnt = 0, vcnt = 0, qn = 0;
+      uint32_t k_used = 0, k_par = 0, v_used = 0, v_par = 0;
+      const uint32_t sq = sQ(g);
+      const int kb = C::B_KFULL + g * C::KST, keb = C::B_KEMPTY + g * C::KST;
+      const int vb = C::B_VFULL + g * C::VST, veb = C::B_VEMPTY + g * C::VST;
+      const uint32_t sk0 = sb + C::OFF_K + (uint32_t)(g * C::KST) * C::TILE_BYTES;
+      const uint32_t sv0 = sb + C::OFF_V + (uint32_t)(g * C::VST) * C::TILE_BYTES;
+      const int nw = sc.n_waves();
+      bool ok = true;
+      for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
+        const int item = sc.item_of(v, w);
+        if (item < 0) continue;
+        int bh, q;
+        sc.decode(item, bh, q);
+        const int jlo = W ? sc.kv_lo(q) : 0, jhi = sc.kv_hi(q);
+        if (qn > 0 && !wait_one(bar(C::B_QEMPTY + g), (qn - 1) & 1, abort_flag, lim,
+                                SITE_P_QEMPTY))
+          break;
+        mbar_arrive_expect_tx(bar(C::B_QFULL + g), C::TILE_BYTES);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sq + c * C::CHUNK_BYTES, &mq, bar(C::B_QFULL + g),
+                      c * C::CHUNK_ELEMS, q * 128, bh);
+        ++qn;
+        for (int j = jlo; j <= jhi && ok; ++j) {
+          {
+            const int s = kcnt % C::KST;
+            const uint32_t ph = (kcnt / C::KST) & 1;
+            if (!wait_one(bar(keb + s), ph ^ 1, abort_flag, lim, SITE_P_KEMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kb + s), C::TILE_BYTES);
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(sk0 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &mk, bar(kb + s),
+                          c * C::CHUNK_ELEMS, j * 128, bh);
+            k_used |= 1u << s;
+            k_par = (k_par & ~(1u << s)) | (ph << s);
+            ++kcnt;
+          }
+          {
+            const int s = vcnt % C::VST;
+            const uint32_t ph = (vcnt / C::VST) & 1;
+            if (!wait_one(bar(veb + s), ph ^ 1, abort_flag, lim, SITE_P_VEMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(vb + s), C::TILE_BYTES);
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(sv0 + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &mv, bar(vb + s),
+                          c * C::CHUNK_ELEMS, j * 128, bh);
+            v_used |= 1u << s;
+            v_par = (v_par & ~(1u << s)) | (ph << s);
+            ++vcnt;
+          }
+        }
+      }
+      // Drain: every copy this thread issued lands before the CTA exits.
+      volatile int no_abort = 0;
+      if (qn > 0)
+        wait_one(bar(C::B_QFULL + g), (qn - 1) & 1, &no_abort, lim, SITE_DRAIN);
+      for (int s = 0; s < C::KST; ++s)
+        if ((k_used >> s) & 1)
+          wait_one(bar(kb + s), (k_par >> s) & 1, &no_abort, lim, SITE_DRAIN);
+      for (int s = 0; s < C::VST; ++s)
+        if ((v_used >> s) & 1)
+          wait_one(bar(vb + s), (v_par >> s) & 1, &no_abort, lim, SITE_DRAIN);
+    }
+    __syncwarp();
+  } else if (!C::SA && warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&mq);
@@ -403,23 +493,21 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
     __syncwarp();
   } else if (C::SA && (warp == kMmaWarp || warp == kMmaWarp1)) {
     // ------------------------------------------------------------ tensor core
-    // (SA) One issuing thread per query block t, so that one thread's barrier
-    // waits and commits overlap the other's products in the tensor pipe
-    // (with S_t(j+1) issued ahead of P_t V_j, neither block waits for the
-    // other's burst).  Both walk every key block of the item: the K/V ring
-    // stages and the Q tiles are released by one commit from each (after
-    // each has seen the stage filled), whether or not its query block reads
-    // that key block.
+    // (SA) Group g's issuing thread: S_g(j+1) as soon as the softmax group
+    // has read S_g(j) (S-free), then P_g V_j once P is written (P-ready), for
+    // the single-block items of worker g*grid + cta, from the group's own
+    // Q tile and K/V ring.
     if (lane == 0) {
-      const int t = warp == kMmaWarp ? 0 : 1;
+      const int g = warp == kMmaWarp ? 0 : 1;
+      const int v = g * (int)gridDim.x + (int)blockIdx.x;
       uint32_t kcnt = 0, vcnt = 0, it = 0;
       uint32_t pc = 0;  // P-ready phases consumed
-      uint32_t si = 0;  // S_t products issued so far
-      // S_t is overwritten only after the softmax group has read the
-      // previous S_t out of TMEM
+      uint32_t si = 0;  // S products issued so far
+      // S_g is overwritten only after the softmax group has read the
+      // previous S_g out of TMEM
       auto s_free = [&]() -> bool {
         if (si > 0) {
-          if (!wait_one(bar(C::B_SFREE + t), (si - 1) & 1, abort_flag, lim,
+          if (!wait_one(bar(C::B_SFREE + g), (si - 1) & 1, abort_flag, lim,
                         SITE_M_SFREE))
             return false;
           tc_fence_after();
@@ -427,113 +515,82 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
         ++si;
         return true;
       };
-      const uint32_t tS = tmem + C::TM_S + 128 * t;
-      const uint32_t tO = tmem + C::TM_O + D * t;
-      const uint32_t tP = tmem + C::TM_P + 64 * t;
+      const uint32_t tS = tmem + C::TM_S + 128 * g;
+      const uint32_t tO = tmem + C::TM_O + D * g;
+      const uint32_t tP = tmem + C::TM_P + 64 * g;
+      const uint32_t sq = sQ(g);
+      const int kb = C::B_KFULL + g * C::KST, keb = C::B_KEMPTY + g * C::KST;
+      const int vb = C::B_VFULL + g * C::VST, veb = C::B_VEMPTY + g * C::VST;
+      const uint32_t sk0 = sb + C::OFF_K + (uint32_t)(g * C::KST) * C::TILE_BYTES;
+      const uint32_t sv0 = sb + C::OFF_V + (uint32_t)(g * C::VST) * C::TILE_BYTES;
       const int nw = sc.n_waves();
       for (int w = 0; w < nw && !*abort_flag; ++w) {
-        const int item = sc.item_of(blockIdx.x, w);
+        const int item = sc.item_of(v, w);
         if (item < 0) continue;
-        int bh;
-        int q0;
-        bool valid1;  // the item holds query block q0 + 1 as well
-        sc.decode_blocks(item, bh, q0, valid1);
-        // key-block range of each query block (tile 1's may start one block
-        // later and ends one later under the causal mask; empty if absent)
-        const int lo0 = W ? sc.kv_lo(q0) : 0, hi0 = sc.kv_hi(q0);
-        const int lo1 = (W && valid1) ? sc.kv_lo(q0 + 1) : 0;
-        const int hi1 = valid1 ? sc.kv_hi(q0 + 1) : -1;
-        const int jlo = lo0, jhi = hi1 > hi0 ? hi1 : hi0;
-        const int lo = t ? lo1 : lo0, hi = t ? hi1 : hi0;
-        auto mine = [&](int j) { return j >= lo && j <= hi; };
-        bool ok = wait_one(bar(C::B_QFULL), it & 1, abort_flag, lim, SITE_M_QFULL);
+        int bh, q;
+        sc.decode(item, bh, q);
+        const int lo = W ? sc.kv_lo(q) : 0, hi = sc.kv_hi(q);
+        bool ok = wait_one(bar(C::B_QFULL + g), it & 1, abort_flag, lim, SITE_M_QFULL);
         if (!ok) break;
         tc_fence_after();
-        {  // S_t for the first key block
+        {  // S for the first key block
           const int s = kcnt % C::KST;
-          if (!wait_one(bar(C::B_KFULL + s), (kcnt / C::KST) & 1, abort_flag,
-                        lim, SITE_M_KFULL))
+          if (!wait_one(bar(kb + s), (kcnt / C::KST) & 1, abort_flag, lim,
+                        SITE_M_KFULL))
             break;
           tc_fence_after();
-          if (mine(jlo)) {
-            if (!s_free()) break;
-            C::mma_s(tS, sQ(t), sb + C::OFF_K + s * C::TILE_BYTES);
-            umma_commit(bar(C::B_SFULL + t));
-          }
-          umma_commit(bar(C::B_KEMPTY + s));
+          if (!s_free()) break;
+          C::mma_s(tS, sq, sk0 + s * C::TILE_BYTES);
+          umma_commit(bar(C::B_SFULL + g));
+          umma_commit(bar(keb + s));
           ++kcnt;
-          // the Q tiles are read by S products only: this thread releases
-          // them after its own last S of the item (here when that was the
-          // first, or when its query block is absent from the item)
-          if (hi == jlo || hi < lo) umma_commit(bar(C::B_QEMPTY));
+          // the Q tile is read by S products only: free after the last one
+          if (hi == lo) umma_commit(bar(C::B_QEMPTY + g));
         }
-        for (int j = jlo; j <= jhi && ok; ++j) {
+        for (int j = lo; j <= hi && ok; ++j) {
           const int vs = vcnt % C::VST;
-          if (!wait_one(bar(C::B_VFULL + vs), (vcnt / C::VST) & 1, abort_flag,
-                        lim, SITE_M_VFULL)) {
+          if (!wait_one(bar(vb + vs), (vcnt / C::VST) & 1, abort_flag, lim,
+                        SITE_M_VFULL)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sv = sb + C::OFF_V + vs * C::TILE_BYTES;
-          const bool next = j + 1 <= jhi;  // the item has key block j + 1
-          const int ks = kcnt % C::KST;
-          const uint32_t sk = sb + C::OFF_K + ks * C::TILE_BYTES;
-          bool k_ready = false;
-          auto k_wait = [&]() -> bool {
-            if (k_ready) return true;
-            if (!wait_one(bar(C::B_KFULL + ks), (kcnt / C::KST) & 1, abort_flag,
-                          lim, SITE_M_KFULL))
-              return false;
-            tc_fence_after();
-            k_ready = true;
-            return true;
-          };
-          // O_t += P_t V_j once the softmax group has written P_t
-          auto do_pv = [&]() -> bool {
-            if (!mine(j)) return true;
-            if (!wait_one(bar(C::B_PREADY + t), pc & 1, abort_flag, lim,
-                          SITE_M_PREADY))
-              return false;
-            ++pc;
-            tc_fence_after();
-            C::mma_pv(tO, tP, sv, j > lo);
-            umma_commit(bar(C::B_PVDONE + t));
-            if (j == hi) umma_commit(bar(C::B_ODONE + t));
-            return true;
-          };
-          // S_t = Q_t K_{j+1}^T
-          auto do_s = [&]() -> bool {
-            if (!mine(j + 1)) return true;
-            if (!k_wait()) return false;
-            if (!s_free()) return false;
-            C::mma_s(tS, sQ(t), sk);
-            umma_commit(bar(C::B_SFULL + t));
-            return true;
-          };
-          // S_t(j+1) first: P_t V_j reads P_t's own columns
-          ok = do_s();
-          if (ok && j + 1 == hi) umma_commit(bar(C::B_QEMPTY));  // its last S
-          ok = ok && do_pv();
-          if (!ok) break;
-          umma_commit(bar(C::B_VEMPTY + vs));
-          ++vcnt;
-          if (next) {  // released only once this thread has seen it filled
-            if (!k_wait()) {
+          if (j + 1 <= hi) {  // S_g(j+1) first: P_g V_j reads P's own columns
+            const int ks = kcnt % C::KST;
+            if (!wait_one(bar(kb + ks), (kcnt / C::KST) & 1, abort_flag, lim,
+                          SITE_M_KFULL) ||
+                !s_free()) {
               ok = false;
               break;
             }
-            umma_commit(bar(C::B_KEMPTY + ks));
+            tc_fence_after();
+            C::mma_s(tS, sq, sk0 + ks * C::TILE_BYTES);
+            umma_commit(bar(C::B_SFULL + g));
+            umma_commit(bar(keb + ks));
             ++kcnt;
+            if (j + 1 == hi) umma_commit(bar(C::B_QEMPTY + g));
           }
+          // O_g += P_g V_j once the softmax group has written P_g
+          if (!wait_one(bar(C::B_PREADY + g), pc & 1, abort_flag, lim,
+                        SITE_M_PREADY)) {
+            ok = false;
+            break;
+          }
+          ++pc;
+          tc_fence_after();
+          C::mma_pv(tO, tP, sv0 + vs * C::TILE_BYTES, j > lo);
+          umma_commit(bar(C::B_PVDONE + g));
+          if (j == hi) umma_commit(bar(C::B_ODONE + g));
+          umma_commit(bar(veb + vs));
+          ++vcnt;
         }
         if (!ok) break;
         ++it;
       }
       // every MMA issued by this thread completes before TMEM is released
-      umma_commit(bar(C::B_MMADONE + t));
+      umma_commit(bar(C::B_MMADONE + g));
       volatile int no_abort = 0;
-      wait_one(bar(C::B_MMADONE + t), 0, &no_abort, lim, SITE_DRAIN);
+      wait_one(bar(C::B_MMADONE + g), 0, &no_abort, lim, SITE_DRAIN);
     }
     __syncwarp();
   } else {
@@ -547,15 +604,21 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
     const float sl2 = p.scale_log2;
     uint32_t scnt = 0, ocnt = 0;
     const int nw = sc.n_waves();
+    // (SA) the group's own worker; otherwise the CTA's pair items
+    const int v = C::SA ? t * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x;
     for (int w = 0; w < nw && !*abort_flag; ++w) {
-      const int item = sc.item_of(blockIdx.x, w);
+      const int item = sc.item_of(v, w);
       if (item < 0) continue;
-      int bh;
-      int q0;
-      bool two;
-      sc.decode_blocks(item, bh, q0, two);
-      if (t == 1 && !two) continue;
-      const int q = q0 + t;
+      int bh, q;
+      if constexpr (C::SA) {
+        sc.decode(item, bh, q);
+      } else {
+        int q0;
+        bool two;
+        sc.decode_blocks(item, bh, q0, two);
+        if (t == 1 && !two) continue;
+        q = q0 + t;
+      }
       const int jlo = W ? sc.kv_lo(q) : 0, jhi = sc.kv_hi(q);
       const int row = q * 128 + wq * 32 + lane;
       float m = -INFINITY;     // running row maximum of the raw scores
@@ -844,8 +907,9 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, void* O,
   p.v_descale = s.v_descale;
   p.drop = s.drop;
   const int BH = s.B * s.H;
-  p.sched = FwdSched::planned(BH, s.N, s.causal, num_sms, s.window);
-  const int grid = p.sched.grid;
+  p.sched = C::SA ? FwdSched::planned_groups(BH, s.N, s.causal, num_sms, s.window)
+                  : FwdSched::planned(BH, s.N, s.causal, num_sms, s.window);
+  const int grid = C::SA ? p.sched.grid / 2 : p.sched.grid;
   fwd_kernel<D, W, DR, E8><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(
       maps.q, maps.k, maps.v, p);
   return cudaGetLastError();

@@ -85,6 +85,19 @@ struct FwdSched {
     return sc;
   }
 
+  // The d = 64 forward's schedule: single-block items for two workers per
+  // CTA (its two query-block groups, worker g * CTAs + cta), so `grid`
+  // counts workers and the launch takes grid / 2 CTAs of at most num_sms.
+  static FwdSched planned_groups(int bh, int n, int is_causal, int num_sms, int win = 0) {
+    FwdSched probe;
+    probe.init(bh, n, is_causal, 2 * num_sms, win, 1);
+    int ctas = (probe.total_items + 1) / 2;
+    if (ctas > num_sms) ctas = num_sms;
+    FwdSched sc;
+    sc.init(bh, n, is_causal, 2 * ctas, win, 1);
+    return sc;
+  }
+
   // Number of waves a CTA walks through.
   __host__ __device__ int n_waves() const {
     return (total_items + grid - 1) / grid;

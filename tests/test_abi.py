@@ -187,29 +187,39 @@ def test_library_has_no_oracle_symbols(L):
     assert b"oracle_" not in data
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 300)])
 @pytest.mark.parametrize("BH,N,sms", [(128, 1024, 152), (128, 1024, 148), (1, 256, 152),
                                       (3, 1000, 152), (5, 129, 152), (64, 4096, 152),
-                                      (4095, 4096, 152), (7, 2048, 2)])
-def test_forward_work_list_covers_every_query_block_once(L, BH, N, sms, causal, window):
+                                      (4095, 4096, 152), (7, 2048, 2), (1, 1, 152)])
+def test_forward_work_list_covers_every_query_block_once(L, BH, N, sms, causal, window, d):
     """The forward launch's work list, walked on the host exactly as the CTAs
-    take it (waves, snake order, head groups, and without a mask the split of
-    a last wave that fills at most half the grid into single query blocks):
-    every (head, 128-row query block) is held by exactly one item."""
-    counts, grid, items = fa.fa_fwd_schedule_cover(BH, N, causal, window, sms)
+    take it (waves, snake order, head groups; at d = 128 pairs of query
+    blocks, without a mask the pairs of a last wave that fills at most half
+    the grid split into single blocks; at d = 64 single blocks for two
+    workers per CTA): every (head, 128-row query block) is held by exactly one
+    item."""
+    counts, grid, items = fa.fa_fwd_schedule_cover(BH, N, causal, window, sms, d)
     assert 1 <= grid <= sms
     assert all(c == 1 for row in counts for c in row)
     nq = (N + 127) // 128
-    assert BH * ((nq + 1) // 2) <= items <= BH * nq
+    if d == 64:
+        assert items == BH * nq
+    else:
+        assert BH * ((nq + 1) // 2) <= items <= BH * nq
 
 
 def test_forward_work_list_splits_the_last_partial_wave(L):
-    """GPT-2 medium shape without a mask on 152 SMs: 512 two-block items make
-    3 waves and 56 items, so those 56 become 112 single-block items and the
-    grid stays at 152."""
-    counts, grid, items = fa.fa_fwd_schedule_cover(128, 1024, False, 0, 152)
+    """128 heads of 1024 rows at d = 128 without a mask on 152 SMs: 512
+    two-block items make 3 waves and 56 items, so those 56 become 112
+    single-block items and the grid stays at 152."""
+    counts, grid, items = fa.fa_fwd_schedule_cover(128, 1024, False, 0, 152, 128)
     assert grid == 152 and all(c == 1 for row in counts for c in row)
     assert items == 3 * 152 + 2 * 56
     # under the causal mask the items differ in cost and none is split
-    _, _, items_c = fa.fa_fwd_schedule_cover(128, 1024, True, 0, 152)
+    _, _, items_c = fa.fa_fwd_schedule_cover(128, 1024, True, 0, 152, 128)
     assert items_c == 512
+    # at d = 64 every item is one query block, for 2 x 152 workers
+    counts, grid, items = fa.fa_fwd_schedule_cover(128, 1024, False, 0, 152, 64)
+    assert grid == 152 and items == 1024
+    assert all(c == 1 for row in counts for c in row)

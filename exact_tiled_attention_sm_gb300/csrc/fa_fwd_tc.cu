@@ -94,8 +94,9 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NRING * KST * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + NRING * VST * TILE_BYTES;
   // barrier slots (the Q and ring barriers of group g at + g under SA)
-  static constexpr int B_QFULL = 0, B_QEMPTY = 2;  // [2]
-  static constexpr int B_KFULL = 4, B_KEMPTY = B_KFULL + NRING * KST;
+  static constexpr int NQ = SA ? 2 : 1;  // Q tiles with barriers of their own
+  static constexpr int B_QFULL = 0, B_QEMPTY = NQ;  // [NQ]
+  static constexpr int B_KFULL = 2 * NQ, B_KEMPTY = B_KFULL + NRING * KST;
   static constexpr int B_VFULL = B_KEMPTY + NRING * KST;
   static constexpr int B_VEMPTY = B_VFULL + NRING * VST;
   static constexpr int B_SFULL = B_VEMPTY + NRING * VST;  // [2]
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(Cfg<D, E8>::THREADS, 1)
   const uint64_t lim = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < C::NQ; ++g) {
       mbar_init(bar(C::B_QFULL + g), 1);
       mbar_init(bar(C::B_QEMPTY + g), 1);
     }

@@ -247,18 +247,18 @@ fa_status fa_fwd_schedule_census_window(int N, int causal, int window,
                                         long long* out);
 
 /* Host-side walk of the forward kernel's work list for BH heads of N rows
- * on a GPU with num_sms SMs, as a launch of fa_fwd at head dimension d (64:
- * single query blocks for the two groups of each CTA; 128: pairs) would
- * plan it: counts[bh * ceil(N/128) + q] is set to the number of work items
- * that hold query block q of head bh (every entry should be 1), *grid and
- * *items (each when not NULL) to the number of CTAs launched and of work
- * items in the list.  counts must hold
+ * on a GPU with num_sms SMs, as a launch of fa_fwd at head dimension d would
+ * plan it (d = 64: single query blocks for the two query-block groups of
+ * each CTA; d = 128: pairs of query blocks).  counts[bh * ceil(N/128) + q]
+ * is set to the number of work items that hold query block q of head bh
+ * (every entry should be 1); *grid and *items, each when not NULL, to the
+ * number of CTAs launched and of items in the list.  counts must hold
  * BH * ceil(N/128) ints.  window > 0 selects a causal sliding window, as in
  * fa_fwd_window.  Pure host arithmetic, no GPU needed.  Returns
- * FA_ERR_INVALID_ARG for BH, N or num_sms below 1, window < 0, a null counts,
- * or an item that would fall outside the tensor, FA_ERR_UNSUPPORTED for d
- * other than 64 and 128.  No counterpart on the pages: it exposes the
- * scheduler so that its cover can be tested. */
+ * FA_ERR_INVALID_ARG for BH, N or num_sms below 1, window < 0, a null
+ * counts, or an item that would fall outside the tensor, and
+ * FA_ERR_UNSUPPORTED for d other than 64 and 128.  No counterpart on the
+ * pages: it exposes the scheduler so that its cover can be tested. */
 fa_status fa_fwd_schedule_cover(int BH, int N, int causal, int window, int d,
                                 int num_sms, int* counts, int* grid, int* items);
 

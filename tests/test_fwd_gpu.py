@@ -121,6 +121,41 @@ def test_bf16_reference_moves_every_block(d, causal):
     assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_d64_one_long_head(causal):
+    """d = 64 with one head of 8192 rows: 64 single-block items for 304
+    workers, so most workers idle and, under the mask, the items range from
+    1 to 64 key blocks.  Rows sampled across the sequence against the
+    oracle."""
+    N, d = 8192, 64
+    x = h.seeded(1, 1, N, d, seed=5150, dtype="bf16")
+    o, lse = run_fwd(x, d ** -0.5, causal)
+    rows = np.array([0, 1, 127, 128, 1000, 4095, 4096, 6001, N - 129, N - 128, N - 1])
+    Q, K, V = (inputs.to_f64(x[n]) for n in ("Q", "K", "V"))
+    O, L = oracle.fwd_rows(Q, K, V, d ** -0.5, causal, rows)
+    A, _ = oracle.fwd_rows(Q, K, np.abs(V), d ** -0.5, causal, rows)
+    # the first causal rows see one or two keys: O is then a row of V, |O|
+    # up to ~4, where bf16 rounding alone exceeds 1e-2 (see the bound below)
+    err = np.abs(o.reshape(-1, d)[rows] - O)
+    assert np.all(err <= np.maximum(h.TOL_O_BF16, rounding_bound(O, A)))
+    assert h.max_abs(lse.reshape(-1)[rows], L) <= h.TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_d64_many_short_heads(causal):
+    """d = 64 with 4 x 64 heads of 130 rows: two query blocks per head (the
+    second of 2 rows), 512 single-block items over the workers, several
+    waves of tiny items.  Every row against the oracle."""
+    B, H, N, d = 4, 64, 130, 64
+    x = h.seeded(B, H, N, d, seed=5151, dtype="bf16")
+    o, lse = run_fwd(x, d ** -0.5, causal)
+    Q, K, V = (inputs.to_f64(x[n]) for n in ("Q", "K", "V"))
+    O, L, bound = bf16_output_bound(Q, K, V, d ** -0.5, causal)
+    # (the first causal rows of each head copy a row of V; see above)
+    assert np.all(np.abs(o - O) <= np.maximum(h.TOL_O_BF16, bound))
+    assert h.max_abs(lse, L) <= h.TOL_LSE_BF16
+
+
 def test_bf16_large_logits_stay_finite():
     """Logits with a range near 58 ("LLM Architecture Refresh [3]",
     section 3): no overflow, no NaN.  Such rows are nearly one-hot, so O
@@ -232,8 +267,13 @@ def bf16_output_bound(Q, K, V, scale, causal):
     sum_k p_k |v_k| is the oracle's forward with |V| as the values."""
     O, L = oracle.fwd(Q, K, V, scale, causal)
     A, _ = oracle.fwd(Q, K, np.abs(V), scale, causal)
-    bound = (2.0 ** -8 + 2e-4) * A + bf16_half_ulp(np.abs(O) + 2.0 ** -8 * A) + 1e-5
-    return O, L, bound
+    return O, L, rounding_bound(O, A)
+
+
+def rounding_bound(O, A):
+    """The bound of bf16_output_bound from the oracle's O and
+    A = sum_k p_k |v_k|."""
+    return (2.0 ** -8 + 2e-4) * A + bf16_half_ulp(np.abs(O) + 2.0 ** -8 * A) + 1e-5
 
 
 @pytest.mark.parametrize("d", [64, 128])

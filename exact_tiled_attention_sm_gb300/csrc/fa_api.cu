@@ -185,7 +185,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O,
         static_cast<const float*>(V), static_cast<float*>(O), LSE, cs));
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
   if ((st = get_encoder()) != FA_OK) return st;
-  fa::TileMaps maps;
+  fa::TileMaps maps{};
   const int BH = B * H;
   if ((st = make_map(&maps.q, Q, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.k, K, BH, N, d)) != FA_OK) return st;
@@ -243,7 +243,7 @@ FA_API fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V,
   s.fp8 = 1;
   s.v_descale = v_descale;
   if ((st = get_encoder()) != FA_OK) return st;
-  fa::TileMaps maps;
+  fa::TileMaps maps{};
   const int BH = B * H;
   if ((st = make_map_u8(&maps.q, Q, BH, N, d)) != FA_OK) return st;
   if ((st = make_map_u8(&maps.k, K, BH, N, d)) != FA_OK) return st;
@@ -326,7 +326,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   }
   if (info.sm_major != 10 || info.sm_minor != 3) return FA_ERR_UNSUPPORTED;
   if ((st = get_encoder()) != FA_OK) return st;
-  fa::TileMaps maps;
+  fa::TileMaps maps{};
   const int BH = B * H;
   if (d == 256) {  // one half of d per work item, 64-query blocks
     if ((st = make_map(&maps.q, Q, BH, N, d, 64)) != FA_OK) return st;
@@ -345,6 +345,9 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   if ((st = make_map(&maps.v, V, BH, N, d)) != FA_OK) return st;
   if ((st = make_map(&maps.dO, dO, BH, N, d)) != FA_OK) return st;
   if ((st = make_map_f32(&maps.dq_acc, dQacc, BH, N, d)) != FA_OK) return st;
+  // dK and dV leave the backward kernel through TMA stores
+  if ((st = make_map(&maps.dk, dK, BH, N, d)) != FA_OK) return st;
+  if ((st = make_map(&maps.dv, dV, BH, N, d)) != FA_OK) return st;
   if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, dQacc, cs))) !=
       FA_OK)
     return st;

@@ -81,7 +81,9 @@ struct Cfg {
   static constexpr int B_DKDVDONE = B_DQFREE + 1;
   static constexpr int B_DKDVFREE = B_DKDVDONE + 1;
   static constexpr int B_MMADONE = B_DKDVFREE + 1;
-  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int B_ESTAGED = B_MMADONE + 1;   // dV or dK tile in the dS buffer
+  static constexpr int B_EREAD = B_ESTAGED + 1;     // ... and read by its TMA store
+  static constexpr int NBAR = B_EREAD + 1;
   static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEM + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4;
@@ -112,7 +114,7 @@ enum : uint32_t {
   SITE_L_KVEMPTY = 1, SITE_L_STAGED, SITE_M_KVFULL, SITE_M_QFULL, SITE_M_DQFREE,
   SITE_M_DSREADY, SITE_M_DKDVFREE, SITE_S_QFULL, SITE_S_SFULL, SITE_Q_DQFULL,
   SITE_E_DKDVDONE, SITE_DRAIN, SITE_ALIGN, SITE_M_PREADY, SITE_S_DPFULL,
-  SITE_M_DOFULL
+  SITE_M_DOFULL, SITE_E_STAGED, SITE_E_READ, SITE_S_EREAD
 };
 
 // Keep words of key row `key` for the 64 queries q_base + (0..63): word c
@@ -259,44 +261,15 @@ __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
   }
 }
 
-// Reads one 128 x D fp32 accumulator (lanes = rows) and stores row r as bf16
-// (times `mult` when MUL).
-template <int D, bool MUL = false>
-__device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
-                                                __nv_bfloat16* out, bool store,
-                                                float mult = 1.f) {
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t v[32];
-    tmem_ld32(tmem_col + 32 * c, v);
-    tmem_ld_wait();
-    reg_fence32(v);
-    uint4 o[4];
-    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float a = __uint_as_float(v[2 * k]), b = __uint_as_float(v[2 * k + 1]);
-      if constexpr (MUL) {
-        a *= mult;
-        b *= mult;
-      }
-      ow[k] = pack_bf16x2(a, b);
-    }
-    if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dst[k] = o[k];
-    }
-  }
-}
-
 template <int D, bool DR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq,
                const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv,
                const __grid_constant__ CUtensorMap mdo,
-               const __grid_constant__ CUtensorMap mdq, const Params p) {
+               const __grid_constant__ CUtensorMap mdq,
+               const __grid_constant__ CUtensorMap mdk,
+               const __grid_constant__ CUtensorMap mdv, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
@@ -332,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_DKDVDONE), 1);
     mbar_init(bar(C::B_DKDVFREE), 256);
     mbar_init(bar(C::B_MMADONE), 1);
+    mbar_init(bar(C::B_ESTAGED), 256);
+    mbar_init(bar(C::B_EREAD), 1);
     *abort_flag = 0;
     if (sb & 1023u) record_timeout(abort_flag, SITE_ALIGN);
     fence_barrier_init();
@@ -664,6 +639,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        // the dS tile doubles as the previous item's dK staging: written
+        // only once that tile's TMA store has read it
+        if (i == sc.q_begin(kb) && it > 0 &&
+            !wait_warp(bar(C::B_EREAD), 1, abort_flag, lim, SITE_S_EREAD)) {
+          ok = false;
+          break;
+        }
         ds_half<D, DR>(tmem_row, smem, lse2 + 128, 2 * grp, 64u * grp, r, scale, pr, kw);
         tmem_st_wait();
         fence_proxy_async_smem();
@@ -708,17 +690,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                      SITE_E_DKDVDONE))
         break;
       tc_fence_after();
-      const bool store = key < N;
-      const size_t rowoff = ((size_t)bh * N + (size_t)(store ? key : 0)) * D;
-      if (grp == 0)
-        store_rows_bf16<D, DR>(tmem_row + C::TM_DV, p.dV + rowoff, store,
-                               p.drop.keep_scale);
-      else
-        store_rows_bf16<D>(tmem_row + C::TM_DK, p.dK + rowoff, store);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DKDVFREE));
+      // dV, then dK, leave through the dS tile (free: the item's last dQ
+      // product has completed) and TMA stores of whole 64-column boxes,
+      // instead of a 2*D-byte row per thread.  Group g converts columns
+      // [g*D/2, (g+1)*D/2) of both; TMEM is released once both are read.
+      {
+        constexpr int NPG = D / 16;  // 16-byte pieces of a row per group
+        constexpr int NL = D / 64;   // 32-column TMEM loads per group
+        uint32_t pv[4 * NPG], pk[4 * NPG];
+        auto grab = [&](uint32_t tcol, uint32_t (&dst)[4 * NPG], float mult) {
+#pragma unroll
+          for (int l = 0; l < NL; ++l) {
+            uint32_t v[32];
+            tmem_ld32(tmem_row + tcol + (D / 2) * grp + 32 * l, v);
+            tmem_ld_wait();
+            reg_fence32(v);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              dst[16 * l + k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mult,
+                                            __uint_as_float(v[2 * k + 1]) * mult);
+          }
+        };
+        grab(C::TM_DV, pv, DR ? p.drop.keep_scale : 1.f);  // kept entries' factor
+        grab(C::TM_DK, pk, 1.f);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DKDVFREE));
+        const bool leader = warp == 0 && lane == 0;
+        // stage this thread's half row, then one thread stores the tile
+        auto put = [&](const uint32_t (&src)[4 * NPG], const CUtensorMap* map,
+                       uint32_t par) {
+#pragma unroll
+          for (int q = 0; q < NPG; ++q)
+            *reinterpret_cast<uint4*>(smem + C::OFF_DS + swz_offset(r, NPG * grp + q)) =
+                make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(bar(C::B_ESTAGED));
+          if (leader &&
+              wait_one(bar(C::B_ESTAGED), par, abort_flag, lim, SITE_E_STAGED)) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)  // rows past N are cut by the copy
+              tma_store_3d(map, sb + C::OFF_DS + c * kChunkBytes, 64 * c, kb * 128, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(bar(C::B_EREAD));
+          }
+        };
+        put(pv, &mdv, 0);
+        if (!wait_warp(bar(C::B_EREAD), 0, abort_flag, lim, SITE_E_READ)) break;
+        put(pk, &mdk, 1);
+      }
       ++it;
     }
+    // the last dK stores complete before the CTA exits
+    if (warp == 0 && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -751,7 +775,7 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   const int grid = total < num_sms ? total : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
   bwd_kernel<D, DR><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, p);
+      maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, maps.dk, maps.dv, p);
   return cudaGetLastError();
 }
 

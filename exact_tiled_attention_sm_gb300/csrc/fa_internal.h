@@ -34,7 +34,7 @@ struct AttnShape {
 // 32-column x 128-row boxes (the backward's bulk reductions); all with the
 // 128-byte swizzle.
 struct TileMaps {
-  CUtensorMap q, k, v, o, dO, dq_acc;
+  CUtensorMap q, k, v, o, dO, dq_acc, dk, dv;
 };
 
 // fa_fwd_tc.cu -- bf16 forward on tcgen05/TMEM.

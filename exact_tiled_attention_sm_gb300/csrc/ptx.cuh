@@ -147,6 +147,18 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map,
       : "memory");
 }
 
+// 3-D tiled store: the box at (x, y, z) of a tiled tensor map from shared
+// memory at src, tracked by this thread's bulk async-group.  Rows past the
+// tensor's end are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src,
+                                             int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group "
+      "[%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

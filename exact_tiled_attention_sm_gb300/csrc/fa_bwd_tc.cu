@@ -261,6 +261,37 @@ __device__ __forceinline__ void ds_half(uint32_t tmem_row, uint8_t* smem,
   }
 }
 
+// Reads one 128 x D fp32 accumulator (lanes = rows) and stores row r as bf16
+// (times `mult` when MUL).
+template <int D, bool MUL = false>
+__device__ __forceinline__ void store_rows_bf16(uint32_t tmem_col,
+                                                __nv_bfloat16* out, bool store,
+                                                float mult = 1.f) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tmem_col + 32 * c, v);
+    tmem_ld_wait();
+    reg_fence32(v);
+    uint4 o[4];
+    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      float a = __uint_as_float(v[2 * k]), b = __uint_as_float(v[2 * k + 1]);
+      if constexpr (MUL) {
+        a *= mult;
+        b *= mult;
+      }
+      ow[k] = pack_bf16x2(a, b);
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dst[k] = o[k];
+    }
+  }
+}
+
 template <int D, bool DR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap mq,
@@ -641,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // the dS tile doubles as the previous item's dK staging: written
         // only once that tile's TMA store has read it
-        if (i == sc.q_begin(kb) && it > 0 &&
+        if (!DR && i == sc.q_begin(kb) && it > 0 &&
             !wait_warp(bar(C::B_EREAD), 1, abort_flag, lim, SITE_S_EREAD)) {
           ok = false;
           break;
@@ -690,15 +721,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                      SITE_E_DKDVDONE))
         break;
       tc_fence_after();
-      // dV, then dK, leave through the dS tile (free: the item's last dQ
-      // product has completed) and TMA stores of whole 64-column boxes,
-      // instead of a 2*D-byte row per thread.  Group g converts columns
-      // [g*D/2, (g+1)*D/2) of both; TMEM is released once both are read.
-      {
+      if constexpr (DR) {  // a row per thread (measured faster with dropout)
+        const bool store = key < N;
+        const size_t rowoff = ((size_t)bh * N + (size_t)(store ? key : 0)) * D;
+        if (grp == 0)
+          store_rows_bf16<D, true>(tmem_row + C::TM_DV, p.dV + rowoff, store,
+                                   p.drop.keep_scale);
+        else
+          store_rows_bf16<D>(tmem_row + C::TM_DK, p.dK + rowoff, store);
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DKDVFREE));
+      } else {
+        // dV, then dK, leave through the dS tile (free: the item's last dQ
+        // product has completed) and TMA stores of whole 64-column boxes,
+        // instead of a 2*D-byte row per thread.  Group g converts columns
+        // [g*D/2, (g+1)*D/2) of both; TMEM is released once both are read.
         constexpr int NPG = D / 16;  // 16-byte pieces of a row per group
         constexpr int NL = D / 64;   // 32-column TMEM loads per group
         uint32_t pv[4 * NPG], pk[4 * NPG];
-        auto grab = [&](uint32_t tcol, uint32_t (&dst)[4 * NPG], float mult) {
+        auto grab = [&](uint32_t tcol, uint32_t (&dst)[4 * NPG]) {
 #pragma unroll
           for (int l = 0; l < NL; ++l) {
             uint32_t v[32];
@@ -707,12 +748,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             reg_fence32(v);
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-              dst[16 * l + k] = pack_bf16x2(__uint_as_float(v[2 * k]) * mult,
-                                            __uint_as_float(v[2 * k + 1]) * mult);
+              dst[16 * l + k] = pack_bf16x2(__uint_as_float(v[2 * k]),
+                                            __uint_as_float(v[2 * k + 1]));
           }
         };
-        grab(C::TM_DV, pv, DR ? p.drop.keep_scale : 1.f);  // kept entries' factor
-        grab(C::TM_DK, pk, 1.f);
+        grab(C::TM_DV, pv);
+        grab(C::TM_DK, pk);
         tc_fence_before();
         mbar_arrive(bar(C::B_DKDVFREE));
         const bool leader = warp == 0 && lane == 0;
@@ -742,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++it;
     }
     // the last dK stores complete before the CTA exits
-    if (warp == 0 && lane == 0) bulk_wait_group0();
+    if (!DR && warp == 0 && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();

@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   FA_TRACE_MARK(g_cta_trace, 0);
   const uint32_t tmem = *tmem_slot;
   const int nw = sc.n_waves();
+  // The dQ conversion launched after this grid may start now: one of its
+  // CTAs fits beside this one and waits (griddep_wait) for this grid to end.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------- loads
@@ -320,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // LSE and D of a block's 64 queries (2 per lane), loaded one block ahead
     // from clamped addresses; validity applied when written to the stage
     float lraw[2] = {0.f, 0.f}, draw[2] = {0.f, 0.f};
+    griddep_wait();  // D comes from the pre-pass launched just before
     auto fetch_stats = [&](int bh_, int i_) {
       const size_t base = (size_t)bh_ * N;
 #pragma unroll
@@ -521,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp - kDqWarp0;  // TMEM lane quarter
     const uint32_t tmem_row = tmem + ((uint32_t)(wq * 32) << 16);
     const int r = wq * 32 + lane;
+    griddep_wait();  // the accumulator is zeroed by the pre-pass
     uint32_t g = 0;
     bool ok = true;
     for (int w = 0; w < nw && ok && !*abort_flag; ++w) {
@@ -783,8 +788,10 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   probe.init(BH, s.N, s.causal, num_sms, s.window);
   const int grid = probe.total_items < num_sms ? probe.total_items : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  bwd256_kernel<DR><<<grid, kThreads, SMEM_BYTES, stream>>>(maps.q, maps.k, maps.dO, p);
-  return cudaGetLastError();
+  // a dependent of the pre-pass launched just before (D, the zeroed dQ
+  // accumulator): its set-up overlaps the pre-pass's last CTAs
+  return launch_after(bwd256_kernel<DR>, dim3(grid), dim3(kThreads), SMEM_BYTES, stream, maps.q,
+                      maps.k, maps.dO, p);
 }
 
 }  // namespace bwd256

@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   FA_TRACE_MARK(g_cta_trace, 0);
   const uint32_t tmem = *tmem_slot;
   const int nw = sc.n_waves();
+  // No early griddep_launch_dependents here: the dQ conversion launched
+  // after this grid starts when it exits (signalling at the start measured
+  // 1% slower at d = 128, where no conversion CTA fits beside this one).
 
   if (warp == kLoadWarp) {
     // ---------------------------------------------------------------- loads
@@ -401,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         draw[e] = p.Dvec[base + q];
       }
     };
+    // D and the zeroed dQ accumulator come from the pre-pass launched just
+    // before this grid: this warp is their only reader (the statistics and
+    // the bulk reduce-adds)
+    griddep_wait();
     // the first block this CTA processes
     for (int w = 0; w < nw; ++w) {
       const int item = sc.item_of(blockIdx.x, w);
@@ -815,9 +822,10 @@ cudaError_t launch(const AttnShape& s, const TileMaps& maps, const float* LSE,
   const int total = BH * n_blk;
   const int grid = total < num_sms ? total : num_sms;
   p.sched.init(BH, s.N, s.causal, grid, s.window);
-  bwd_kernel<D, DR><<<grid, kThreads, C::SMEM_BYTES, stream>>>(
-      maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, maps.dk, maps.dv, p);
-  return cudaGetLastError();
+  // a dependent of the pre-pass launched just before (D, the zeroed dQ
+  // accumulator): its set-up overlaps the pre-pass's last CTAs
+  return launch_after(bwd_kernel<D, DR>, dim3(grid), dim3(kThreads), C::SMEM_BYTES, stream,
+                      maps.q, maps.k, maps.v, maps.dO, maps.dq_acc, maps.dk, maps.dv, p);
 }
 
 }  // namespace bwdtc

@@ -44,6 +44,30 @@ cudaError_t smem_limit_once(Kern kernel, int bytes,
   return e;
 }
 
+// Launches `kernel` as a programmatic dependent of the launch before it on
+// `stream`: its CTAs may start once every CTA of that launch has signalled
+// (griddep_launch_dependents) or exited, so its launch and set-up overlap the
+// other's last CTAs.  The kernel must call griddep_wait before it touches
+// anything the earlier launch writes; everything older than that launch is
+// complete when it starts.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  const cudaError_t last = cudaGetLastError();  // read and clear, as after <<<>>>
+  return e != cudaSuccess ? e : last;
+}
+
 }  // namespace fa
 
 // Defines `unsigned int NAME(cudaStream_t)` that synchronises the stream,

@@ -285,6 +285,9 @@ __global__ void __launch_bounds__(256)
     bwd_pre_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                    float* __restrict__ Dv, float* __restrict__ dQacc,
                    long long rows) {
+  // the backward kernel after this launch reads D and the zeroed
+  // accumulator only after its griddep_wait, which waits for all of this grid
+  griddep_launch_dependents();
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -328,6 +331,7 @@ __global__ void __launch_bounds__(128)
 __global__ void __launch_bounds__(256)
     dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                       long long n4) {
+  griddep_wait();  // the backward kernel launched before has finished dQacc
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 v = src[i];
@@ -455,9 +459,8 @@ cudaError_t launch_dq_convert(const AttnShape& s, const float* dQacc, void* dQ,
   long long blocks = (n4 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  simt::dq_convert_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(dQacc), reinterpret_cast<uint2*>(dQ), n4);
-  return cudaGetLastError();
+  return launch_after(simt::dq_convert_kernel, dim3((unsigned)blocks), dim3(256), 0, stream,
+                      reinterpret_cast<const float4*>(dQacc), reinterpret_cast<uint2*>(dQ), n4);
 }
 
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, cudaStream_t stream) {

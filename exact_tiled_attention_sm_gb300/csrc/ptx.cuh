@@ -31,6 +31,17 @@ __device__ __forceinline__ uint32_t lane_id() {
   return l;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Waits until the launches this grid depends on have completed and their
+// memory is visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// This CTA no longer holds back the launch that depends on this grid.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)

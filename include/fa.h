@@ -85,6 +85,12 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * accumulator; per key block, recompute S and P from LSE, dV += P^T dO,
  * dP = dO V^T, dS = P*(dP - D), dK += scale*dS^T Q, dQacc += scale*dS K
  * (fp32 bulk reduce-adds); dQ = dQacc converted to the input dtype.
+ * In bf16 the call is three launches on `stream` (D and the zeroed
+ * accumulator; the backward kernel; the conversion).  The second and third
+ * are programmatic dependent launches: each may start while the one before
+ * it ends and waits on the device for that one's results.  Work queued on
+ * `stream` before the call, or after it, is ordered against the whole call
+ * as usual, stream capture included.
  * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG for a short workspace. */
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O,
                  const void* dO, const float* LSE, void* dQ, void* dK,

@@ -1,10 +1,11 @@
-"""The forward and the backward captured into a CUDA graph: the backward's
-three launches (D and the zeroed accumulator, the backward kernel, the dQ
-conversion) are chained as programmatic dependent launches, and a graph keeps
-those edges.  Replays must give the eager results: O, LSE, dK and dV bit for
-bit (no launch-order-dependent arithmetic), dQ (fp32 reduce-adds whose order
-varies between launches) within rounding, and all of them against the fp64
-oracle."""
+"""The forward and the backward captured into a CUDA graph (causal, sliding
+window, dropout; d = 64, 128, 256): the backward's three launches (D and the
+zeroed accumulator, the backward kernel, the dQ conversion) are chained as
+programmatic dependent launches, and a graph keeps those edges.  Replays must
+give the eager results: O, LSE, dK and dV bit for bit (no
+launch-order-dependent arithmetic), dQ (fp32 reduce-adds whose order varies
+between launches) within rounding, and, without dropout, the fp64 oracle's
+gradients."""
 import pytest
 import torch
 
@@ -16,11 +17,16 @@ from tests import helpers as h
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_fwd_bwd_graph_replay_matches_eager(d):
+@pytest.mark.parametrize("d,window,dropout_p", [
+    (64, 0, 0.0), (128, 0, 0.0), (256, 0, 0.0),  # causal
+    (128, 300, 0.0), (256, 300, 0.0),             # sliding window of 300 keys
+    (128, 0, 0.1), (256, 0, 0.1),                 # causal with dropout
+])
+def test_fwd_bwd_graph_replay_matches_eager(d, window, dropout_p):
     B, H, N, causal = 1, 4, 700, True
     sc = d ** -0.5
-    x = h.seeded(B, H, N, d, seed=900 + d, dtype="bf16", with_dO=True)
+    seed = 77
+    x = h.seeded(B, H, N, d, seed=900 + d + window, dtype="bf16", with_dO=True)
     q, k, v, do = (x[n].to("cuda") for n in ("Q", "K", "V", "dO"))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
@@ -28,8 +34,10 @@ def test_fwd_bwd_graph_replay_matches_eager(d):
     ws = fa.workspace(B, H, N, d)
 
     def step():
-        fa.fwd(q, k, v, sc, causal, out=o, lse=lse)
-        fa.bwd(q, k, v, o, do, lse, sc, causal, dq=dq, dk=dk, dv=dv, ws=ws)
+        fa.fwd(q, k, v, sc, causal, out=o, lse=lse, window=window, dropout_p=dropout_p,
+               seed=seed)
+        fa.bwd(q, k, v, o, do, lse, sc, causal, dq=dq, dk=dk, dv=dv, ws=ws, window=window,
+               dropout_p=dropout_p, seed=seed)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -55,7 +63,9 @@ def test_fwd_bwd_graph_replay_matches_eager(d):
         assert torch.isfinite(dq.float()).all()
         assert h.rel_l2(h.np64(dq), h.np64(eager[2])) <= 1e-3
 
+    if dropout_p:  # the dropout paths' own parity tests compare them with the oracle
+        return
     Q, K, V, dO = (inputs.to_f64(x[n]) for n in ("Q", "K", "V", "dO"))
-    dQr, dKr, dVr, _ = oracle.bwd(Q, K, V, dO, sc, causal)
+    dQr, dKr, dVr, _ = oracle.bwd(Q, K, V, dO, sc, causal, window=window)
     for got, ref in ((dq, dQr), (dk, dKr), (dv, dVr)):
         assert h.rel_l2(h.np64(got), ref) <= h.TOL_GRAD_REL

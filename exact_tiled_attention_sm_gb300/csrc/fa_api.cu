@@ -351,10 +351,13 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O,
   if ((st = from_cuda(fa::launch_bwd_pre(s, O, dO, 1, Dvec, dQacc, cs))) !=
       FA_OK)
     return st;
-  if ((st = from_cuda(fa::launch_bwd_tc(s, maps, LSE, Dvec, dQacc, dK, dV,
-                                        info.num_sms, fa::kWaitLimitNs, cs))) !=
-      FA_OK)
-    return st;
+  const cudaError_t ke =
+      (d == 64 && s.drop.t4 == 0)
+          ? fa::launch_bwd64_tc(s, maps, LSE, Dvec, dK, dV, info.num_sms,
+                                fa::kWaitLimitNs, cs)
+          : fa::launch_bwd_tc(s, maps, LSE, Dvec, dQacc, dK, dV, info.num_sms,
+                              fa::kWaitLimitNs, cs);
+  if ((st = from_cuda(ke)) != FA_OK) return st;
   return from_cuda(fa::launch_dq_convert(s, dQacc, dQ, cs));
 }
 
@@ -397,9 +400,10 @@ FA_API fa_status fa_bwd_dropout(const void* Q, const void* K, const void* V,
 
 FA_API fa_status fa_last_device_status(void* stream) {
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const unsigned int words[5] = {fa::read_status_fwd_tc(cs),
+  const unsigned int words[6] = {fa::read_status_fwd_tc(cs),
                                  fa::read_status_fwd256_tc(cs),
                                  fa::read_status_bwd_tc(cs),
+                                 fa::read_status_bwd64_tc(cs),
                                  fa::read_status_bwd256_tc(cs),
                                  fa::read_status_simt(cs)};
   fa_status out = FA_OK;

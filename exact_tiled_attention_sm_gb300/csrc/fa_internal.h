@@ -56,6 +56,15 @@ cudaError_t launch_bwd_tc(const AttnShape& s, const TileMaps& maps,
                           uint64_t wait_limit_ns, cudaStream_t stream);
 unsigned int read_status_bwd_tc(cudaStream_t stream);
 
+// fa_bwd64_tc.cu -- bf16 backward for d = 64 without dropout (dQ with TMEM
+// columns and a shared-memory staging ring of its own); the maps and the
+// zeroed accumulator (maps.dq_acc) are fa_bwd_tc's.
+cudaError_t launch_bwd64_tc(const AttnShape& s, const TileMaps& maps,
+                            const float* LSE, const float* Dvec, void* dK,
+                            void* dV, int num_sms, uint64_t wait_limit_ns,
+                            cudaStream_t stream);
+unsigned int read_status_bwd64_tc(cudaStream_t stream);
+
 // fa_bwd256_tc.cu -- bf16 backward for d = 256 on tcgen05/TMEM.  maps.q and
 // maps.dO must have 64-row boxes (64 queries per block), maps.k 128-row ones;
 // V is read directly (into TMEM); dQacc is the fp32 accumulator, zeroed.

@@ -5,14 +5,15 @@ Marshalling and arithmetic on recorded times only; the attention itself runs
 in the trace build's kernels exactly as in libfa.so."""
 import ctypes
 
-READERS = {"fwd": "fa_cta_trace_fwd", "bwd": "fa_cta_trace_bwd",
+READERS = {"fwd": "fa_cta_trace_fwd", "bwd": "fa_cta_trace_bwd", "bwd64": "fa_cta_trace_bwd64",
            "fwd256": "fa_cta_trace_fwd256", "bwd256": "fa_cta_trace_bwd256"}
 MAX_CTAS = 1024  # kTraceMaxCtas in csrc/fa_trace.cuh
 
 
 def read(lib, kernel):
     """(start, end) in ns of every CTA of the last traced launch of `kernel`
-    ("fwd", "bwd", "fwd256" or "bwd256"), then cleared on the device."""
+    ("fwd", "bwd", "bwd64", "fwd256" or "bwd256"), then cleared on the
+    device."""
     buf = (ctypes.c_ulonglong * (2 * MAX_CTAS))()
     fn = getattr(lib, READERS[kernel])
     fn.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]

@@ -281,7 +281,9 @@ def run_balance(args):
         runs = []
         for rep in range(6):
             call()
-            marks = trace.read(L, which + ("256" if w.d == 256 else ""))
+            # the kernel that ran: d = 256 and (backward) d = 64 have their own
+            marks = trace.read(L, which + ("256" if w.d == 256 else
+                                           "64" if (w.d == 64 and which == "bwd") else ""))
             if rep >= 3:
                 runs.append(trace.summarize(marks))
         st = fa.last_device_status()
